@@ -1,0 +1,570 @@
+#!/usr/bin/env python3
+"""CSA decode benchmark on B300: query-tokens/s and HBM GB/s of one decode step of B = 32 requests
+at N = 65,536 (one query each at t = N - 1: compress-on-close, indexer, top-k 512, sparse attention
+over window 128 + 512 selected entries, sink, inverse RoPE), plus the 8K causal prefill (TFLOP/s).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0. Under torchrun (N > 1) every rank runs its own 32 requests
+(weak scaling, no data-path collective); the timed region is bracketed by a barrier and a device
+synchronise on both sides and the max over ranks is reported. `--impl reference` times the fp64
+NumPy oracle on the host cores on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+DECODE_WL = synth.WORKLOADS[1]
+PREFILL_WL = synth.WORKLOADS[2]
+ROTATIONS = 3                      # input copies cycled between steps (defeats the 126 MB L2)
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+    except (OSError, ValueError):
+        d = dict(FALLBACK_PEAKS)
+        d["source"] = "fallback"
+    return d
+
+
+# ----------------------------------------------------------------------------- work accounting
+def decode_work(wl: synth.Workload, B: int) -> dict:
+    """Algorithmic bytes / flops of one decode step of B requests (what the method must move:
+    the visible index cache, the gathered candidate rows, q / q_idx / w / sink, the output, and the
+    closing group of the compressor). Score round-trips and split partials are overhead, excluded."""
+    es = 2 if wl.storage == "bf16" else 4
+    t, m = wl.t, wl.ratio
+    V = (t + 1) // m
+    n_win = min(wl.window, t + 1)
+    n_comp = V if wl.hca else min(wl.top_k, V)
+    C = n_win + n_comp
+    idx_bytes = 0 if wl.hca else B * (V * wl.d_idx * es + wl.H_idx * wl.d_idx * es + wl.H_idx * 4)
+    kv_bytes = B * C * wl.d * es
+    q_bytes = B * wl.H * wl.d * es + wl.H * 4
+    out_bytes = B * wl.H * wl.d * es
+    close = (t + 1) % m == 0
+    chans = wl.d + (0 if wl.hca else wl.d_idx)
+    comp_bytes = B * (2 * m * chans * 2 * es + chans * es) if close else 0
+    flops_idx = 0 if wl.hca else 2 * B * wl.H_idx * wl.d_idx * V
+    flops_attn = 4 * B * wl.H * C * wl.d
+    return {"bytes": idx_bytes + kv_bytes + q_bytes + out_bytes + comp_bytes, "index_bytes": idx_bytes,
+            "flops": flops_idx + flops_attn, "flops_index": flops_idx, "flops_attn": flops_attn}
+
+
+def prefill_flops(wl: synth.Workload) -> dict:
+    t = np.arange(wl.S, dtype=np.int64)
+    V = (t + 1) // wl.ratio
+    idx = 0 if wl.hca else int(2 * wl.H_idx * wl.d_idx * V.sum())
+    comp = V if wl.hca else np.minimum(wl.top_k, V)
+    attn = int(4 * wl.H * wl.d * (comp + np.minimum(wl.window, t + 1)).sum())
+    return {"index": wl.B * idx, "attn": wl.B * attn, "total": wl.B * (idx + attn)}
+
+
+# ----------------------------------------------------------------------------- clocks during the run
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples: list[tuple[float, list[str]]] = []
+        self.err = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError as e:
+            self.proc, self.err = None, str(e)
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"unavailable": self.err}
+        inside = [s for ts, s in self.samples if t0 <= ts <= t1]
+        note = "in timed region"
+        if not inside:                           # region shorter than the sampling period
+            near = sorted(self.samples, key=lambda x: min(abs(x[0] - t0), abs(x[0] - t1)))[:2]
+            inside = [s for _, s in near]
+            note = "nearest samples (timed region shorter than the 100 ms sampling period)"
+        if not inside:
+            return {"unavailable": "no nvidia-smi samples"}
+        sm = [float(s[1]) for s in inside if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in inside if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in inside for n, v in zip(names, s[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "note": note}
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- device inputs
+def device_inputs(wl: synth.Workload, requests, device):
+    """Draws the requests (host threads) and uploads them into [B, ...] device tensors as they
+    are drawn, so the host never holds the whole batch."""
+    import torch
+    B = len(requests)
+    dt = torch.bfloat16 if wl.storage == "bf16" else torch.float32
+    T = {"kv": torch.empty(B, wl.N, wl.d, dtype=dt, device=device),
+         "gate": torch.empty(B, wl.N, wl.d, dtype=dt, device=device),
+         "q": torch.empty(B, wl.S, wl.H, wl.d, dtype=dt, device=device)}
+    if not wl.hca:
+        T["idx_k"] = torch.empty(B, wl.N, wl.d_idx, dtype=dt, device=device)
+        T["idx_gate"] = torch.empty(B, wl.N, wl.d_idx, dtype=dt, device=device)
+        T["q_idx"] = torch.empty(B, wl.S, wl.H_idx, wl.d_idx, dtype=dt, device=device)
+        T["w"] = torch.empty(B, wl.S, wl.H_idx, dtype=torch.float32, device=device)
+    slot = {b: i for i, b in enumerate(requests)}
+
+    def up(b, r):
+        i = slot[b]
+        for k, v in r.items():
+            if v is None:
+                continue
+            if k == "w" or wl.storage == "f32":
+                src = torch.from_numpy(np.ascontiguousarray(v, np.float32))
+            else:
+                src = torch.from_numpy(synth.bf16_bits(v).view(np.int16)).view(torch.bfloat16)
+            T[k][i].copy_(src)
+        return None
+
+    synth.gen_requests(wl, requests, fn=up)
+    sh = synth.gen_shared(wl)
+    T["bias"] = torch.from_numpy(sh["bias"]).to(device)
+    T["sink"] = torch.from_numpy(sh["sink"]).to(device)
+    if not wl.hca:
+        T["idx_bias"] = torch.from_numpy(sh["idx_bias"]).to(device)
+    torch.cuda.synchronize()
+    return T
+
+
+def make_cfg(wl):
+    import long_context_sparse_19_b300 as L
+    return L.Config(H=wl.H, d=wl.d, d_rope=wl.d_rope, H_idx=wl.H_idx, d_idx=wl.d_idx, ratio=wl.ratio,
+                    top_k=wl.top_k, window=wl.window, storage=wl.storage)
+
+
+def make_cache(T, wl, device):
+    import torch
+    import long_context_sparse_19_b300 as L
+    B = T["kv"].shape[0]
+    dt = T["kv"].dtype
+    ckv = torch.empty(B, wl.n_entries, wl.d, dtype=dt, device=device)
+    cidx = None if wl.hca else torch.empty(B, wl.n_entries, wl.d_idx, dtype=dt, device=device)
+    return L.Cache(kv=T["kv"], gate=T["gate"], gate_bias=T["bias"], ckv=ckv, idx_k=T.get("idx_k"),
+                   idx_gate=T.get("idx_gate"), idx_bias=T.get("idx_bias"), cidx=cidx)
+
+
+# ----------------------------------------------------------------------------- our decode leg
+def run_decode(args, world, rank, device, peaks) -> dict:
+    import torch
+    import long_context_sparse_19_b300 as L
+    wl = DECODE_WL
+    B = wl.B
+    cfg = make_cfg(wl)
+    t_setup = time.time()
+    T = device_inputs(wl, list(range(rank * B, rank * B + B)), device)
+    cache = make_cache(T, wl, device)
+    L.csa_compress(cfg, cache, 0, wl.n_entries)            # the caches the decode step reads
+    pos = torch.full((B,), wl.t, dtype=torch.int64, device=device)
+    rot = []
+    for r in range(ROTATIONS):
+        if r == 0:
+            c, q, qi, w = cache, T["q"][:, 0].contiguous(), T["q_idx"][:, 0].contiguous(), T["w"][:, 0].contiguous()
+        else:
+            c = L.Cache(kv=cache.kv.clone(), gate=cache.gate.clone(), gate_bias=cache.gate_bias,
+                        ckv=cache.ckv.clone(), idx_k=cache.idx_k.clone(), idx_gate=cache.idx_gate.clone(),
+                        idx_bias=cache.idx_bias, cidx=cache.cidx.clone())
+            q, qi, w = rot[0]["q"].clone(), rot[0]["q_idx"].clone(), rot[0]["w"].clone()
+        out = torch.empty(B, wl.H, wl.d, dtype=cache.kv.dtype, device=device)
+        ws = L.workspace(cfg, B, 1, wl.n_entries, device=device)
+        rot.append({"cache": c, "q": q, "q_idx": qi, "w": w, "out": out, "pos": pos.clone(), "ws": ws})
+        rot[-1]["call"] = L.binding.bind_decode(cfg, rot[-1]["pos"], c, q, qi, w, T["sink"], out, ws=ws)
+    torch.cuda.synchronize()
+    setup_s = time.time() - t_setup
+
+    # CUDA graph of one decode step per input copy (the C-ABI call captured on the capture stream)
+    for r in rot:
+        r["call"]()
+    torch.cuda.synchronize()
+    n0 = L.csa_launch_count()
+    graphs = []
+    for r in rot:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            r["call"]()
+        graphs.append(g)
+    launches_per_step = (L.csa_launch_count() - n0) // ROTATIONS
+    assert L.csa_get_device_status() == 0
+
+    for i in range(args.warmup):
+        graphs[i % ROTATIONS].replay()
+    K = args.steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(gpu_ident(device))
+    time.sleep(0.25)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    ev0.record()
+    for i in range(K):
+        graphs[i % ROTATIONS].replay()
+    ev1.record()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier(world)
+    clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, world)
+    clk = clocks.summary(wall0, wall1)
+
+    # Second pass, same steps without the graph, with a CUDA event pair around every kernel on its
+    # launching stream: per-kernel average durations for the roofline.
+    L.csa_profile_begin(K * launches_per_step + 16)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(K):
+        rot[i % ROTATIONS]["call"]()
+    e1.record()
+    torch.cuda.synchronize()
+    prof = L.csa_profile_end()
+    eager_ms = e0.elapsed_time(e1)
+
+    # End to end: per step, the step's inputs (q, q_idx, w, the new token's raw rows) come from
+    # pinned host memory and the output goes back to pinned host memory, all inside the region.
+    e2e = run_e2e(args, wl, rot, world, device)
+    assert L.csa_get_device_status() == 0
+
+    work = decode_work(wl, B)
+    idx_ms, idx_n = prof["index"]
+    idx_avg_s = idx_ms / max(idx_n, 1) / 1e3
+    achieved = work["index_bytes"] / idx_avg_s / 1e9 if idx_n else None
+    step_s = ms_max / K / 1e3
+    qtok = world * B * K / (ms_max / 1e3)
+    res = {
+        "value": qtok, "ms_per_step": ms_max / K, "hbm_gbs": work["bytes"] / step_s / 1e9,
+        "hbm_frac_of_measured": work["bytes"] / step_s / 1e9 / peaks["hbm_gbs"],
+        "step_bytes": work["bytes"], "step_flops": work["flops"], "gpu_launches": launches_per_step * K,
+        "clocks": clk, "setup_s": round(setup_s, 1), "eager_ms_per_step": eager_ms / K,
+        "stages_ms_per_step": {k: round(v[0] / K, 5) for k, v in prof.items()},
+        "stage_launches": {k: v[1] for k, v in prof.items()},
+        "roofline": {"kernel": "indexer scores (csa_index_topk / csa_decode stage 1)", "bound": "hbm",
+                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": (achieved / peaks["hbm_gbs"]) if achieved else None, "traffic": None,
+                     "algorithmic_bytes_per_launch": work["index_bytes"],
+                     "avg_launch_us": idx_avg_s * 1e6, "peak_source": peaks["source"]},
+        "e2e": e2e,
+    }
+    return res
+
+
+def gpu_ident(device) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(torch.cuda.current_device())
+
+
+def run_e2e(args, wl, rot, world, device) -> dict:
+    import torch
+    B, t = wl.B, wl.t
+    dt = rot[0]["q"].dtype
+    host = []
+    for r in rot:
+        c = r["cache"]
+        hb = {"q": r["q"].cpu().pin_memory(), "q_idx": r["q_idx"].cpu().pin_memory(),
+              "w": r["w"].cpu().pin_memory(), "pos": r["pos"].cpu().pin_memory(),
+              "kv": c.kv[:, t].cpu().pin_memory(), "gate": c.gate[:, t].cpu().pin_memory(),
+              "idx_k": c.idx_k[:, t].cpu().pin_memory(), "idx_gate": c.idx_gate[:, t].cpu().pin_memory(),
+              "out": torch.empty((B, wl.H, wl.d), dtype=dt).pin_memory()}
+        host.append(hb)
+    h2d = sum(host[0][k].numel() * host[0][k].element_size()
+              for k in ("q", "q_idx", "w", "pos", "kv", "gate", "idx_k", "idx_gate"))
+    d2h = host[0]["out"].numel() * host[0]["out"].element_size()
+
+    def step(i):
+        r, hb = rot[i % ROTATIONS], host[i % ROTATIONS]
+        c = r["cache"]
+        r["q"].copy_(hb["q"], non_blocking=True)
+        r["q_idx"].copy_(hb["q_idx"], non_blocking=True)
+        r["w"].copy_(hb["w"], non_blocking=True)
+        r["pos"].copy_(hb["pos"], non_blocking=True)
+        c.kv[:, t].copy_(hb["kv"], non_blocking=True)
+        c.gate[:, t].copy_(hb["gate"], non_blocking=True)
+        c.idx_k[:, t].copy_(hb["idx_k"], non_blocking=True)
+        c.idx_gate[:, t].copy_(hb["idx_gate"], non_blocking=True)
+        r["call"]()
+        hb["out"].copy_(r["out"], non_blocking=True)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    K = args.steps
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        step(i)
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t0
+    barrier(world)
+    el = max_over_ranks(el, world)
+    return {"value": world * B * K / el, "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": el / K * 1e3}
+
+
+# ----------------------------------------------------------------------------- prefill leg
+def run_prefill(args, device, peaks) -> dict:
+    import torch
+    import long_context_sparse_19_b300 as L
+    wl = PREFILL_WL
+    cfg = make_cfg(wl)
+    T = device_inputs(wl, list(range(wl.B)), device)
+    cache = make_cache(T, wl, device)
+    out = torch.empty(wl.B, wl.S, wl.H, wl.d, dtype=cache.kv.dtype, device=device)
+    ws = L.workspace(cfg, wl.B, wl.S, wl.n_entries, device=device)
+
+    def call():
+        L.csa_prefill(cfg, cache, T["q"], T["q_idx"], T["w"], T["sink"], out, ws=ws)
+
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    reps = args.prefill_reps
+    L.csa_profile_begin(reps * 8 + 8)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    prof = L.csa_profile_end()
+    assert L.csa_get_device_status() == 0
+    ms = e0.elapsed_time(e1) / reps
+    fl = prefill_flops(wl)
+    pk = peaks["bf16_tflops"]
+    idx_ms = prof["index"][0] / reps
+    attn_ms = prof["attn"][0] / reps
+    return {"workload": wl.name, "ms": ms, "tflops": fl["total"] / ms / 1e9, "flops": fl["total"],
+            "index": {"ms": idx_ms, "tflops": fl["index"] / idx_ms / 1e9 if idx_ms else None,
+                      "frac_of_bf16_peak": fl["index"] / idx_ms / 1e9 / pk if idx_ms else None},
+            "attn": {"ms": attn_ms, "tflops": fl["attn"] / attn_ms / 1e9 if attn_ms else None,
+                     "frac_of_bf16_peak": fl["attn"] / attn_ms / 1e9 / pk if attn_ms else None},
+            "stages_ms": {k: round(v[0] / reps, 4) for k, v in prof.items()},
+            "peak_tflops": pk, "peak_source": peaks["source"]}
+
+
+# ----------------------------------------------------------------------------- the oracle on the host
+def oracle_setup(wl, requests):
+    """fp64 caches of the sampled requests, built by the oracle itself (not timed)."""
+    from oracle import csa_oracle as O
+    sh = synth.gen_shared(wl)
+    o = O.OracleConfig(H=wl.H, d=wl.d, d_rope=wl.d_rope, H_idx=wl.H_idx, d_idx=wl.d_idx, ratio=wl.ratio,
+                       top_k=wl.top_k, window=wl.window)
+    items = []
+    for b in requests:
+        r = synth.gen_request(wl, b)
+        n = wl.n_entries
+        ckv = O.compress(r["kv"], r["gate"], sh["bias"], wl.ratio, n)
+        cidx = None if wl.hca else O.compress(r["idx_k"], r["idx_gate"], sh["idx_bias"], wl.ratio, n)
+        items.append((r, ckv, cidx))
+    return o, sh, items
+
+
+def oracle_step(o, sh, item, t):
+    """One decode step of one request in the oracle: compress-on-close of entry t//m, then
+    indexer, top-k and sparse attention."""
+    from oracle import csa_oracle as O
+    r, ckv, cidx = item
+    m = o.ratio
+    if (t + 1) % m == 0:
+        e = t // m
+        lo, hi = (e - 1) * m, (e + 1) * m
+        for src, g, bias, cache in ((r["kv"], r["gate"], sh["bias"], ckv),
+                                    (r["idx_k"], r["idx_gate"], sh["idx_bias"], cidx)):
+            if cache is None:
+                continue
+            x = O.pool_window(src[lo:hi], g[lo:hi], bias)
+            cache[e] = O.rope(O.rms_norm(x, o.rms_eps), e * m, o.d_rope, o.rope_base)
+    return O.decode_step(t, r["q"][0], None if o.hca else r["q_idx"][0], None if o.hca else r["w"][0],
+                         sh["sink"], r["kv"], ckv, cidx, o)
+
+
+def host_cores() -> dict:
+    info = {"affinity_cores": len(os.sched_getaffinity(0))}
+    try:
+        from threadpoolctl import threadpool_info
+        info["blas_threads"] = max((p.get("num_threads", 1) for p in threadpool_info()), default=1)
+    except Exception:
+        info["blas_threads"] = None
+    return info
+
+
+def run_cpu_baseline(budget_s: float, n_req: int = 2) -> dict:
+    wl = DECODE_WL
+    o, sh, items = oracle_setup(wl, list(range(n_req)))
+    oracle_step(o, sh, items[0], wl.t)                    # warm-up
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(o, sh, items[done % n_req], wl.t)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    hc = host_cores()
+    return {"value": done / el, "unit": "query-tokens/s", "cores": hc["blas_threads"] or hc["affinity_cores"],
+            "kind": "oracle", "host": hc,
+            "sample": f"{done} single-request decode steps (requests 0..{n_req - 1} of the B=32, N=65,536 "
+                      f"workload, fp64 NumPy; caches prebuilt untimed), {el:.1f} s; matmuls use the BLAS "
+                      f"threads, element-wise NumPy one thread"}
+
+
+def run_reference(args, world, rank) -> None:
+    if rank != 0:
+        return
+    wl = DECODE_WL
+    n_req = 2
+    o, sh, items = oracle_setup(wl, list(range(n_req)))
+    for i in range(args.warmup):
+        oracle_step(o, sh, items[i % n_req], wl.t)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_step(o, sh, items[i % n_req], wl.t)
+    el = time.perf_counter() - t0
+    hc = host_cores()
+    v = args.steps / el
+    line = {"metric": METRIC, "impl": "reference", "value": v, "unit": "query-tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": decode_config(world),
+            "cpu_baseline": {"value": v, "unit": "query-tokens/s", "kind": "oracle",
+                             "cores": hc["blas_threads"] or hc["affinity_cores"],
+                             "sample": f"each step = one request's decode step (requests 0..{n_req - 1} of the "
+                                       f"workload), fp64 NumPy oracle on the host; caches prebuilt untimed"},
+            "e2e": {"value": v, "unit": "query-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "CSA decode query-tokens/s (N=65,536, B=32, H=64, top-k 512, W=128, bf16)"
+
+
+def decode_config(world) -> dict:
+    wl = DECODE_WL
+    return {"workload": wl.name, "B_per_gpu": wl.B, "N": wl.N, "t": wl.t, "H": wl.H, "H_idx": wl.H_idx,
+            "top_k": wl.top_k, "window": wl.window, "ratio": wl.ratio, "parallelism": f"requests x{world}",
+            "l2": f"inputs rotated over {ROTATIONS} device copies (~{ROTATIONS * 153} MB touched per cycle "
+                  f"> 126 MB L2)", "timing": "CUDA graph of one csa_decode call per step, CUDA events"}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--prefill-reps", type=int, default=3)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    world, rank, local = dist_setup()
+    device = torch.device("cuda", torch.cuda.current_device())
+    peaks = load_peaks()
+    # the host-side oracle baseline runs first (rank 0, N = 1), before the GPU is busy
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline(args.cpu_budget)
+    dec = run_decode(args, world, rank, device, peaks)
+    pre = None if args.no_prefill else run_prefill(args, device, peaks)
+    if rank == 0:
+        line = {"metric": METRIC, "value": dec["value"], "unit": "query-tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": dec["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": decode_config(world),
+                "hbm_gbs": dec["hbm_gbs"], "hbm_frac_of_measured": dec["hbm_frac_of_measured"],
+                "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
+                "gpu_launches": dec["gpu_launches"], "clocks": dec["clocks"],
+                "detail": {k: dec[k] for k in ("step_bytes", "step_flops", "eager_ms_per_step",
+                                               "stages_ms_per_step", "stage_launches", "setup_s")},
+                "prefill": pre}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,191 @@
+/*
+ * csa.h — C ABI of the compressed-sparse-attention (CSA / HCA) hot path.
+ *
+ * The operations follow the DeepSeek-V4-Flash attention as described in
+ *   [FLASH] "DeepSeek-V4-Flash 架构：一个 token 的旅程" (hs-black.github.io/posts/deepseek-v4-flash)
+ *   [LAB41] "Lab tổng hợp DeepSeek-V4.1-Flash — chạy toàn trình 1A → 6B bằng NumPy" (openarchlab.com)
+ *   [ATLAS] "LLM Atlas — DeepSeek" (llm-atlas.k1412.top/deepseek), section 19
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every tensor pointer is caller-owned DEVICE memory, dense row-major (last index fastest),
+ *    at least 16-byte aligned. Storage tensors (raw kv / gates / keys, caches, q, out) have the
+ *    dtype csa_config.storage (float32 or bfloat16); gate biases, indexer weights, sinks and
+ *    scores are float32; positions are int64; selected indices are int32.
+ *  - No call allocates device memory. Temporary buffers live in the caller's workspace
+ *    (ws, ws_bytes), sized by csa_workspace_bytes(); the workspace must not be shared by calls
+ *    that may run concurrently.
+ *  - Every call only enqueues work on `stream` and returns without synchronising. Arguments are
+ *    checked before anything is launched; on an argument error nothing is written and the
+ *    status says why (csa_last_error() gives a one-line message for the calling thread).
+ *  - A device-side problem detected by a kernel (an index outside the cache, a bounded wait that
+ *    ran out) sets a per-device error word instead of trapping; csa_get_device_status() reads it.
+ *  - Positions are absolute token indices t. A query at t may read compressed entries
+ *    i < (t + 1) / ratio ([FLASH] "压缩条目必须等整组完成后才可见") and raw tokens
+ *    max(0, t - window + 1) .. t.
+ *  - q and q_idx are passed before RoPE; the library rotates them at t.
+ */
+#ifndef CSA_H_
+#define CSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CSA_OK = 0,
+  CSA_ERR_INVALID_ARG = 1,     /* null pointer, negative size, misaligned pointer          */
+  CSA_ERR_SHAPE = 2,           /* unsupported or inconsistent shape                         */
+  CSA_ERR_DTYPE = 3,           /* unsupported storage dtype                                 */
+  CSA_ERR_WORKSPACE = 4,       /* ws_bytes smaller than csa_workspace_bytes()               */
+  CSA_ERR_CUDA = 5,            /* a CUDA runtime call or launch failed                      */
+  CSA_ERR_DEVICE = 6,          /* a kernel reported a device-side error (see error word)    */
+  CSA_ERR_NOT_IMPLEMENTED = 7  /* valid request that this build does not support            */
+} csa_status;
+
+typedef enum { CSA_F32 = 0, CSA_BF16 = 1 } csa_dtype;
+
+/* csa_config.flags */
+#define CSA_FLAG_SIMT 1u       /* use the CUDA-core kernels even where a tcgen05 kernel exists */
+
+/* Shape and hyper-parameters of one layer (tensor contract of [FLASH] "每个算子先对齐四个维度").
+ * Supported: d = 512, d_rope = 64, d_idx = 128, 1 <= H <= 64, 1 <= H_idx <= 64,
+ * 1 <= ratio <= 256, 0 <= top_k <= 2048 (0 = HCA, every visible entry), 1 <= window <= 1024. */
+typedef struct {
+  int32_t H;             /* query heads                                                  */
+  int32_t d;             /* width of the single shared KV head (K = V), 512               */
+  int32_t d_rope;        /* rotary tail width, 64 (the last d_rope dims are rotated)       */
+  int32_t H_idx;         /* indexer heads                                                */
+  int32_t d_idx;         /* indexer width, 128                                            */
+  int32_t ratio;         /* compression ratio m (CSA 4, HCA 128)                          */
+  int32_t top_k;         /* selected compressed entries per query; 0 = HCA                */
+  int32_t window;        /* raw sliding-window length W                                   */
+  float rope_base;       /* RoPE base, 10000                                              */
+  float softmax_scale;   /* attention logit scale; <= 0 selects 1/sqrt(d)                 */
+  float rms_eps;         /* RMSNorm epsilon after pooling, 1e-6                           */
+  csa_dtype storage;     /* storage dtype of kv, gates, keys, caches, q, q_idx, out       */
+  uint32_t flags;        /* CSA_FLAG_*                                                    */
+} csa_config;
+
+/* Raw per-token inputs and compressed caches of B requests.
+ *   kv, gate        [B, N, d]        storage   raw shared KV head rows and compressor gate logits
+ *   gate_bias       [2*ratio, d]     float32   positional gate bias, index p = j - (i-1)*ratio
+ *   idx_k, idx_gate [B, N, d_idx]    storage   raw index keys and their gate logits (NULL for HCA)
+ *   idx_bias        [2*ratio, d_idx] float32   (NULL for HCA)
+ *   ckv             [B, n_cap, d]    storage   compressed KV cache (entry i rotated at i*ratio)
+ *   cidx            [B, n_cap, d_idx] storage  compressed index cache (NULL for HCA)          */
+typedef struct {
+  const void* kv;
+  const void* gate;
+  const float* gate_bias;
+  const void* idx_k;
+  const void* idx_gate;
+  const float* idx_bias;
+  int64_t N;             /* raw tokens held per request (row stride of kv / gate / idx_*)   */
+  void* ckv;
+  void* cidx;
+  int64_t n_cap;         /* compressed entries held per request (row stride of ckv / cidx) */
+} csa_cache;
+
+/* One-line description of a status code (static storage). */
+const char* csa_status_string(csa_status s);
+
+/* Message of the last argument error raised in the calling thread ("" if none). */
+const char* csa_last_error(void);
+
+/* Reads (and with reset != 0 clears) the device error word of the current device after
+ * synchronising `stream`. Returns CSA_OK or CSA_ERR_DEVICE; *code (nullable) receives the
+ * raw word (0 = no error; otherwise a CSA_DEVERR_* value from the kernels). */
+csa_status csa_get_device_status(cudaStream_t stream, int reset, int32_t* code);
+
+/* Workspace bytes needed by csa_index_topk / csa_sparse_attn / csa_decode / csa_prefill for
+ * B requests, S queries per request and a compressed capacity of n_cap entries. Returns 0 for
+ * an invalid configuration. */
+size_t csa_workspace_bytes(const csa_config* cfg, int32_t B, int32_t S, int64_t n_cap);
+
+/* Compressor ([FLASH] "压缩是逐通道的 learned pooling", "一个通道，逐项算出压缩结果").
+ * Writes entries i in [first_entry, first_entry + n_entries) of every request:
+ *   for each channel c, softmax over p in [0, 2m) of gate[j, c] + gate_bias[p, c] with
+ *   j = (i-1)m + p (rows j < 0 take weight 0), pooled kv[j, c]; then RMSNorm over the channels
+ *   (unit weight, eps = rms_eps); then RoPE of the last d_rope dims at position i*m.
+ * The same rule builds cidx from idx_k / idx_gate / idx_bias when those are non-NULL.
+ * Requires (first_entry + n_entries) * ratio <= cache->N and first_entry + n_entries <= n_cap. */
+csa_status csa_compress(const csa_config* cfg, int32_t B, const csa_cache* cache,
+                        int64_t first_entry, int64_t n_entries, cudaStream_t stream);
+
+/* Indexer and selection ([FLASH] "少读 KV 之前，Indexer 仍要给历史打分").
+ *   pos     [B, S] int64     query positions t
+ *   q_idx   [B, S, H_idx, d_idx] storage (before RoPE; rotated at t inside)
+ *   w       [B, S, H_idx] float32 signed head weights
+ *   cidx    [B, n_cap, d_idx] storage
+ *   topk    [B, S, top_k] int32 out: the top_k visible entries by
+ *           s_i = sum_h w_h * max(0, rope(q_h, t) . cidx_i), ordered by (-s_i, i); when fewer than
+ *           top_k entries are visible, the tail holds -1.
+ *   scores  [B, S, n_cap] float32 out, nullable: s_i for i < visible(t); other entries untouched.
+ * Requires top_k > 0. */
+csa_status csa_index_topk(const csa_config* cfg, int32_t B, int32_t S, const int64_t* pos,
+                          const void* q_idx, const float* w, const void* cidx, int64_t n_cap,
+                          int32_t* topk, float* scores, void* ws, size_t ws_bytes,
+                          cudaStream_t stream);
+
+/* Sparse joint attention with sink and inverse RoPE ([FLASH] "局部和压缩记忆，共用一次归一化",
+ * "输出投影也分组，并且降低中间维度"; [LAB41] "attn_sink"; HCA: [ATLAS] section 19).
+ *   pos   [B, S] int64; q [B, S, H, d] storage (before RoPE)
+ *   kv    [B, N, d] raw rows; candidate raw token j is kv[j] rotated at j
+ *   ckv   [B, n_cap, d]; topk [B, S, top_k] int32 (-1 = empty slot), or NULL when top_k == 0 (HCA:
+ *         every visible entry is a candidate)
+ *   sink  [H] float32 per-head sink logit (adds exp(sink_h) to the denominator, owns no value)
+ *   out   [B, S, H, d] storage: o_h = sum_c exp(l_hc) e_c / (exp(sink_h) + sum_c exp(l_hc)) with
+ *         l_hc = softmax_scale * rope(q_h, t) . e_c, then rotated back by -t.
+ * A selected index outside [0, visible(t)) is skipped and flagged in the device error word. */
+csa_status csa_sparse_attn(const csa_config* cfg, int32_t B, int32_t S, const int64_t* pos,
+                           const void* q, const void* kv, int64_t N, const void* ckv, int64_t n_cap,
+                           const int32_t* topk, const float* sink, void* out, void* ws,
+                           size_t ws_bytes, cudaStream_t stream);
+
+/* One decode step of B requests, one query each at pos[b] ([FLASH] "压缩条目必须等整组完成后才可见"):
+ * the caller has already written token t = pos[b] into the raw rows of `cache`. If t closes a
+ * group ((t + 1) % ratio == 0) entry t / ratio of ckv (and cidx) is written first; then the
+ * indexer, top-k (skipped for HCA) and the sparse attention run for the query at t.
+ *   pos   [B] int64 (device); q [B, H, d]; q_idx [B, H_idx, d_idx]; w [B, H_idx] (NULL for HCA)
+ *   out   [B, H, d] storage; topk_out [B, top_k] int32, nullable (the selection used). */
+csa_status csa_decode(const csa_config* cfg, int32_t B, const int64_t* pos, const csa_cache* cache,
+                      const void* q, const void* q_idx, const float* w, const float* sink,
+                      void* out, int32_t* topk_out, void* ws, size_t ws_bytes,
+                      cudaStream_t stream);
+
+/* Causal prefill of S = cache->N tokens at positions 0 .. S-1 of B requests: every compressed
+ * entry 0 .. S/ratio - 1 is built at once, then each query t keeps its own visibility mask
+ * ([FLASH] "压缩条目必须等整组完成后才可见": prefill computes all entries in parallel, and each
+ * query still applies its causal mask).
+ *   q [B, S, H, d]; q_idx [B, S, H_idx, d_idx]; w [B, S, H_idx]; out [B, S, H, d];
+ *   topk_out [B, S, top_k] int32, nullable. */
+csa_status csa_prefill(const csa_config* cfg, int32_t B, int32_t S, const csa_cache* cache,
+                       const void* q, const void* q_idx, const float* w, const float* sink,
+                       void* out, int32_t* topk_out, void* ws, size_t ws_bytes,
+                       cudaStream_t stream);
+
+/* ---- Instrumentation (host side; never changes results) -------------------------------------
+ * Stage ids used below: 0 compressor, 1 indexer scores, 2 top-k, 3 sparse attention, 4 split merge. */
+
+/* Number of kernel launches this library has issued in the process so far. */
+int64_t csa_launch_count(void);
+
+/* Starts recording a CUDA event pair on the launching stream around each kernel launch of every
+ * following call (at most max_launches launches are recorded; later ones are counted only).
+ * Not for use while a stream is being captured into a CUDA graph. */
+csa_status csa_profile_begin(int32_t max_launches);
+
+/* Stops recording, waits for the recorded events, and writes for each stage s < n_stages the total
+ * device milliseconds ms[s] and the launch count launches[s] (either pointer may be NULL). */
+csa_status csa_profile_end(float* ms, int32_t* launches, int32_t n_stages);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_H_ */

@@ -1,0 +1,289 @@
+"""Thin ctypes binding of ``libcsa.so`` (the C ABI declared in ``include/csa.h``).
+
+Each function has the C name, takes torch tensors that already live on the GPU, checks that their
+shapes / dtypes / contiguity match the call, and passes raw device pointers plus the current CUDA
+stream. Every step of the computation runs in the library's CUDA kernels; if the library cannot be
+loaded, importing this module raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_char_p, c_float, c_int, c_int32, c_int64, c_size_t, c_uint32, c_void_p
+from dataclasses import dataclass
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcsa.so")
+
+CSA_F32, CSA_BF16 = 0, 1
+CSA_FLAG_SIMT = 1
+
+# the public entry points declared in include/csa.h
+EXPORTS = ("csa_status_string", "csa_last_error", "csa_get_device_status", "csa_workspace_bytes",
+           "csa_compress", "csa_index_topk", "csa_sparse_attn", "csa_decode", "csa_prefill",
+           "csa_launch_count", "csa_profile_begin", "csa_profile_end")
+STAGES = ("compress", "index", "topk", "attn", "merge")
+
+
+class CsaConfig(ctypes.Structure):
+    _fields_ = [("H", c_int32), ("d", c_int32), ("d_rope", c_int32), ("H_idx", c_int32),
+                ("d_idx", c_int32), ("ratio", c_int32), ("top_k", c_int32), ("window", c_int32),
+                ("rope_base", c_float), ("softmax_scale", c_float), ("rms_eps", c_float),
+                ("storage", c_int32), ("flags", c_uint32)]
+
+
+class CsaCache(ctypes.Structure):
+    _fields_ = [("kv", c_void_p), ("gate", c_void_p), ("gate_bias", c_void_p), ("idx_k", c_void_p),
+                ("idx_gate", c_void_p), ("idx_bias", c_void_p), ("N", c_int64), ("ckv", c_void_p),
+                ("cidx", c_void_p), ("n_cap", c_int64)]
+
+
+class CsaError(RuntimeError):
+    def __init__(self, status: int, where: str, msg: str):
+        super().__init__(f"{where}: status {status} ({msg})")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libcsa.so once and declares the prototypes of every exported call."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python long_context_sparse_19_b300/build.py`")
+    L = ctypes.CDLL(path)
+    cp, vp = POINTER(CsaConfig), c_void_p
+    L.csa_status_string.argtypes, L.csa_status_string.restype = [c_int], c_char_p
+    L.csa_last_error.argtypes, L.csa_last_error.restype = [], c_char_p
+    L.csa_get_device_status.argtypes, L.csa_get_device_status.restype = [vp, c_int, POINTER(c_int32)], c_int
+    L.csa_workspace_bytes.argtypes, L.csa_workspace_bytes.restype = [cp, c_int32, c_int32, c_int64], c_size_t
+    L.csa_compress.argtypes, L.csa_compress.restype = [cp, c_int32, POINTER(CsaCache), c_int64, c_int64, vp], c_int
+    L.csa_index_topk.argtypes = [cp, c_int32, c_int32, vp, vp, vp, vp, c_int64, vp, vp, vp, c_size_t, vp]
+    L.csa_index_topk.restype = c_int
+    L.csa_sparse_attn.argtypes = [cp, c_int32, c_int32, vp, vp, vp, c_int64, vp, c_int64, vp, vp, vp, vp,
+                                  c_size_t, vp]
+    L.csa_sparse_attn.restype = c_int
+    L.csa_decode.argtypes = [cp, c_int32, vp, POINTER(CsaCache), vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
+    L.csa_decode.restype = c_int
+    L.csa_prefill.argtypes = [cp, c_int32, c_int32, POINTER(CsaCache), vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
+    L.csa_prefill.restype = c_int
+    L.csa_launch_count.argtypes, L.csa_launch_count.restype = [], c_int64
+    L.csa_profile_begin.argtypes, L.csa_profile_begin.restype = [c_int32], c_int
+    L.csa_profile_end.argtypes, L.csa_profile_end.restype = [POINTER(c_float), POINTER(c_int32), c_int32], c_int
+    _lib = L
+    return L
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        L = load()
+        raise CsaError(status, where, (L.csa_last_error() or b"").decode() or
+                       L.csa_status_string(status).decode())
+
+
+# ------------------------------------------------------------------------------------ config
+@dataclass
+class Config:
+    """Python mirror of csa_config (see include/csa.h)."""
+    H: int = 64
+    d: int = 512
+    d_rope: int = 64
+    H_idx: int = 64
+    d_idx: int = 128
+    ratio: int = 4
+    top_k: int = 512
+    window: int = 128
+    rope_base: float = 10000.0
+    softmax_scale: float = 0.0
+    rms_eps: float = 1e-6
+    storage: str = "bf16"
+    simt: bool = False
+
+    @property
+    def dtype(self) -> torch.dtype:
+        return torch.bfloat16 if self.storage == "bf16" else torch.float32
+
+    def c(self) -> CsaConfig:
+        return CsaConfig(self.H, self.d, self.d_rope, self.H_idx, self.d_idx, self.ratio, self.top_k,
+                         self.window, self.rope_base, self.softmax_scale, self.rms_eps,
+                         CSA_BF16 if self.storage == "bf16" else CSA_F32,
+                         CSA_FLAG_SIMT if self.simt else 0)
+
+
+def _ptr(t, shape=None, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+@dataclass
+class Cache:
+    """Device tensors of the raw per-token inputs and compressed caches of B requests."""
+    kv: torch.Tensor                # [B, N, d]
+    gate: torch.Tensor              # [B, N, d]
+    gate_bias: torch.Tensor         # [2m, d] float32
+    ckv: torch.Tensor               # [B, n_cap, d]
+    idx_k: torch.Tensor | None = None      # [B, N, d_idx]
+    idx_gate: torch.Tensor | None = None
+    idx_bias: torch.Tensor | None = None   # [2m, d_idx] float32
+    cidx: torch.Tensor | None = None       # [B, n_cap, d_idx]
+
+    def c(self, cfg: Config) -> CsaCache:
+        B, N, _ = self.kv.shape
+        n_cap = self.ckv.shape[1]
+        dt = cfg.dtype
+        m = cfg.ratio
+        k = CsaCache()
+        k.kv = _ptr(self.kv, (B, N, cfg.d), dt, "kv")
+        k.gate = _ptr(self.gate, (B, N, cfg.d), dt, "gate")
+        k.gate_bias = _ptr(self.gate_bias, (2 * m, cfg.d), torch.float32, "gate_bias")
+        k.ckv = _ptr(self.ckv, (B, n_cap, cfg.d), dt, "ckv")
+        if self.idx_k is not None:
+            k.idx_k = _ptr(self.idx_k, (B, N, cfg.d_idx), dt, "idx_k")
+            k.idx_gate = _ptr(self.idx_gate, (B, N, cfg.d_idx), dt, "idx_gate")
+            k.idx_bias = _ptr(self.idx_bias, (2 * m, cfg.d_idx), torch.float32, "idx_bias")
+            k.cidx = _ptr(self.cidx, (B, n_cap, cfg.d_idx), dt, "cidx")
+        k.N, k.n_cap = N, n_cap
+        return k
+
+
+# ------------------------------------------------------------------------------------ entry points
+def csa_status_string(status: int) -> str:
+    return load().csa_status_string(status).decode()
+
+
+def csa_get_device_status(reset: bool = True, stream=None) -> int:
+    """Synchronises the stream and returns the device error word (0 = no error)."""
+    code = c_int32(0)
+    load().csa_get_device_status(_stream(stream), int(reset), ctypes.byref(code))
+    return code.value
+
+
+def csa_workspace_bytes(cfg: Config, B: int, S: int, n_cap: int) -> int:
+    return int(load().csa_workspace_bytes(ctypes.byref(cfg.c()), B, S, n_cap))
+
+
+def workspace(cfg: Config, B: int, S: int, n_cap: int, device="cuda") -> torch.Tensor:
+    return torch.empty(max(16, csa_workspace_bytes(cfg, B, S, n_cap)), dtype=torch.uint8, device=device)
+
+
+def csa_compress(cfg: Config, cache: Cache, first_entry: int, n_entries: int, stream=None) -> None:
+    B = cache.kv.shape[0]
+    _check(load().csa_compress(ctypes.byref(cfg.c()), B, ctypes.byref(cache.c(cfg)), first_entry, n_entries,
+                               _stream(stream)), "csa_compress")
+
+
+def csa_index_topk(cfg: Config, pos, q_idx, w, cidx, topk, scores=None, ws=None, stream=None) -> None:
+    B, S = pos.shape
+    n_cap = cidx.shape[1]
+    ws = workspace(cfg, B, S, n_cap) if ws is None else ws
+    _check(load().csa_index_topk(
+        ctypes.byref(cfg.c()), B, S, _ptr(pos, (B, S), torch.int64, "pos"),
+        _ptr(q_idx, (B, S, cfg.H_idx, cfg.d_idx), cfg.dtype, "q_idx"), _ptr(w, (B, S, cfg.H_idx), torch.float32, "w"),
+        _ptr(cidx, (B, n_cap, cfg.d_idx), cfg.dtype, "cidx"), n_cap,
+        _ptr(topk, (B, S, cfg.top_k), torch.int32, "topk"), _ptr(scores, (B, S, n_cap), torch.float32, "scores"),
+        _ptr(ws, None, torch.uint8, "ws"), ws.numel(), _stream(stream)), "csa_index_topk")
+
+
+def csa_sparse_attn(cfg: Config, pos, q, kv, ckv, topk, sink, out, ws=None, stream=None) -> None:
+    B, S = pos.shape
+    N, n_cap = kv.shape[1], ckv.shape[1]
+    ws = workspace(cfg, B, S, n_cap) if ws is None else ws
+    _check(load().csa_sparse_attn(
+        ctypes.byref(cfg.c()), B, S, _ptr(pos, (B, S), torch.int64, "pos"),
+        _ptr(q, (B, S, cfg.H, cfg.d), cfg.dtype, "q"), _ptr(kv, (B, N, cfg.d), cfg.dtype, "kv"), N,
+        _ptr(ckv, (B, n_cap, cfg.d), cfg.dtype, "ckv"), n_cap,
+        _ptr(topk, (B, S, cfg.top_k), torch.int32, "topk") if cfg.top_k else None,
+        _ptr(sink, (cfg.H,), torch.float32, "sink"), _ptr(out, (B, S, cfg.H, cfg.d), cfg.dtype, "out"),
+        _ptr(ws, None, torch.uint8, "ws"), ws.numel(), _stream(stream)), "csa_sparse_attn")
+
+
+def csa_decode(cfg: Config, pos, cache: Cache, q, q_idx, w, sink, out, topk_out=None, ws=None,
+               stream=None) -> None:
+    B = pos.shape[0]
+    n_cap = cache.ckv.shape[1]
+    ws = workspace(cfg, B, 1, n_cap) if ws is None else ws
+    hca = cfg.top_k == 0
+    _check(load().csa_decode(
+        ctypes.byref(cfg.c()), B, _ptr(pos, (B,), torch.int64, "pos"), ctypes.byref(cache.c(cfg)),
+        _ptr(q, (B, cfg.H, cfg.d), cfg.dtype, "q"),
+        None if hca else _ptr(q_idx, (B, cfg.H_idx, cfg.d_idx), cfg.dtype, "q_idx"),
+        None if hca else _ptr(w, (B, cfg.H_idx), torch.float32, "w"),
+        _ptr(sink, (cfg.H,), torch.float32, "sink"), _ptr(out, (B, cfg.H, cfg.d), cfg.dtype, "out"),
+        _ptr(topk_out, (B, cfg.top_k), torch.int32, "topk_out"),
+        _ptr(ws, None, torch.uint8, "ws"), ws.numel(), _stream(stream)), "csa_decode")
+
+
+def csa_prefill(cfg: Config, cache: Cache, q, q_idx, w, sink, out, topk_out=None, ws=None,
+                stream=None) -> None:
+    B, S = q.shape[0], q.shape[1]
+    n_cap = cache.ckv.shape[1]
+    ws = workspace(cfg, B, S, n_cap) if ws is None else ws
+    hca = cfg.top_k == 0
+    _check(load().csa_prefill(
+        ctypes.byref(cfg.c()), B, S, ctypes.byref(cache.c(cfg)),
+        _ptr(q, (B, S, cfg.H, cfg.d), cfg.dtype, "q"),
+        None if hca else _ptr(q_idx, (B, S, cfg.H_idx, cfg.d_idx), cfg.dtype, "q_idx"),
+        None if hca else _ptr(w, (B, S, cfg.H_idx), torch.float32, "w"),
+        _ptr(sink, (cfg.H,), torch.float32, "sink"), _ptr(out, (B, S, cfg.H, cfg.d), cfg.dtype, "out"),
+        _ptr(topk_out, (B, S, cfg.top_k), torch.int32, "topk_out"),
+        _ptr(ws, None, torch.uint8, "ws"), ws.numel(), _stream(stream)), "csa_prefill")
+
+
+def csa_launch_count() -> int:
+    return int(load().csa_launch_count())
+
+
+def csa_profile_begin(max_launches: int) -> None:
+    _check(load().csa_profile_begin(max_launches), "csa_profile_begin")
+
+
+def csa_profile_end() -> dict:
+    """{stage: (total device ms, launches)} of the launches recorded since csa_profile_begin."""
+    n = len(STAGES)
+    ms = (c_float * n)()
+    cnt = (c_int32 * n)()
+    _check(load().csa_profile_end(ms, cnt, n), "csa_profile_end")
+    return {STAGES[i]: (float(ms[i]), int(cnt[i])) for i in range(n)}
+
+
+def bind_decode(cfg: Config, pos, cache: Cache, q, q_idx, w, sink, out, topk_out=None, ws=None):
+    """csa_decode with every argument marshalled once; the returned callable enqueues one decode
+    step on the current stream (so it can be replayed or captured into a CUDA graph cheaply)."""
+    B = pos.shape[0]
+    n_cap = cache.ckv.shape[1]
+    ws = workspace(cfg, B, 1, n_cap) if ws is None else ws
+    hca = cfg.top_k == 0
+    c = cfg.c()
+    k = cache.c(cfg)
+    args = (ctypes.byref(c), B, _ptr(pos, (B,), torch.int64, "pos"), ctypes.byref(k),
+            _ptr(q, (B, cfg.H, cfg.d), cfg.dtype, "q"),
+            None if hca else _ptr(q_idx, (B, cfg.H_idx, cfg.d_idx), cfg.dtype, "q_idx"),
+            None if hca else _ptr(w, (B, cfg.H_idx), torch.float32, "w"),
+            _ptr(sink, (cfg.H,), torch.float32, "sink"), _ptr(out, (B, cfg.H, cfg.d), cfg.dtype, "out"),
+            _ptr(topk_out, (B, cfg.top_k), torch.int32, "topk_out"),
+            _ptr(ws, None, torch.uint8, "ws"), ws.numel())
+    fn = load().csa_decode
+    keep = (c, k, ws)
+
+    def call(stream=None):
+        _ = keep
+        _check(fn(*args, _stream(stream)), "csa_decode")
+    return call

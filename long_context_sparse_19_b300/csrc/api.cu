@@ -1,0 +1,459 @@
+// C ABI of the CSA / HCA path: argument checks, workspace carving, kernel dispatch.
+// Every entry point only enqueues kernels on the caller's stream; nothing here allocates.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/csa.h"
+#include "kernels.h"
+#include "tc.h"
+
+namespace {
+
+using namespace csa;
+
+thread_local std::string g_last_error;
+
+__device__ int32_t g_device_error;      // per-device error word (first error wins)
+
+int32_t* device_error_word() {
+  static std::mutex mu;
+  static int32_t* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<int32_t*>(p);
+  }
+  return addr[dev];
+}
+
+csa_status fail(csa_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+csa_status fail(csa_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+csa_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return CSA_OK;
+  return fail(CSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define CHECK_PTR(p)                                                                       \
+  do {                                                                                     \
+    if (!(p)) return fail(CSA_ERR_INVALID_ARG, "%s is NULL", #p);                          \
+    if (!aligned16(p)) return fail(CSA_ERR_INVALID_ARG, "%s is not 16-byte aligned", #p);  \
+  } while (0)
+
+#define CHECK_OPT_PTR(p)                                                                   \
+  do {                                                                                     \
+    if ((p) && !aligned16(p)) return fail(CSA_ERR_INVALID_ARG, "%s is not 16-byte aligned", #p); \
+  } while (0)
+
+csa_status check_config(const csa_config* c) {
+  if (!c) return fail(CSA_ERR_INVALID_ARG, "cfg is NULL");
+  if (c->storage != CSA_F32 && c->storage != CSA_BF16) return fail(CSA_ERR_DTYPE, "storage dtype %d", (int)c->storage);
+  if (c->d != 512) return fail(CSA_ERR_SHAPE, "d = %d (supported: 512)", c->d);
+  if (c->d_rope != 64) return fail(CSA_ERR_SHAPE, "d_rope = %d (supported: 64)", c->d_rope);
+  if (c->H < 1 || c->H > 64) return fail(CSA_ERR_SHAPE, "H = %d (supported: 1..64)", c->H);
+  if (c->ratio < 1 || c->ratio > 256) return fail(CSA_ERR_SHAPE, "ratio = %d (supported: 1..256)", c->ratio);
+  if (c->top_k < 0 || c->top_k > 2048) return fail(CSA_ERR_SHAPE, "top_k = %d (supported: 0..2048)", c->top_k);
+  if (c->window < 1 || c->window > 1024) return fail(CSA_ERR_SHAPE, "window = %d (supported: 1..1024)", c->window);
+  if (c->top_k > 0) {
+    if (c->d_idx != 128) return fail(CSA_ERR_SHAPE, "d_idx = %d (supported: 128)", c->d_idx);
+    if (c->H_idx < 1 || c->H_idx > 64) return fail(CSA_ERR_SHAPE, "H_idx = %d (supported: 1..64)", c->H_idx);
+  }
+  if (!(c->rope_base > 0.f)) return fail(CSA_ERR_INVALID_ARG, "rope_base must be > 0");
+  if (!(c->rms_eps >= 0.f)) return fail(CSA_ERR_INVALID_ARG, "rms_eps must be >= 0");
+  return CSA_OK;
+}
+
+RopeTab make_rope(const csa_config* c) {
+  RopeTab r;
+  memset(&r, 0, sizeof r);
+  r.d_rope = c->d_rope;
+  for (int i = 0; i < c->d_rope / 2; ++i) r.theta[i] = pow((double)c->rope_base, -2.0 * i / c->d_rope);
+  return r;
+}
+
+float softmax_scale(const csa_config* c) {
+  return c->softmax_scale > 0.f ? c->softmax_scale : (float)(1.0 / sqrt((double)c->d));
+}
+
+bool use_tc(const csa_config* c) {
+  return tc_enabled() && c->storage == CSA_BF16 && !(c->flags & CSA_FLAG_SIMT) && c->H == 64 &&
+         (c->top_k == 0 || c->H_idx == 64);
+}
+
+// ------------------------------------------------------------------ launch counting / stage profiling
+enum Stage { ST_COMPRESS = 0, ST_INDEX = 1, ST_TOPK = 2, ST_ATTN = 3, ST_MERGE = 4, ST_COUNT = 5 };
+
+std::atomic<int64_t> g_launches{0};
+
+struct ProfRec {
+  int stage;
+  cudaEvent_t a, b;
+};
+
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  int cap = 0;
+  std::vector<ProfRec> recs;
+  std::vector<cudaEvent_t> pool;
+  int extra[ST_COUNT] = {0};     // launches counted beyond the recording cap
+} g_prof;
+
+// Wraps one kernel launch: counts it and, while profiling, brackets it with an event pair.
+template <typename F>
+cudaError_t launch_stage(int stage, cudaStream_t st, F&& f) {
+  ProfRec rec{stage, nullptr, nullptr};
+  bool recorded = false;
+  {
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    if (g_prof.on) {
+      if ((int)g_prof.recs.size() < g_prof.cap && g_prof.pool.size() >= 2) {
+        rec.a = g_prof.pool.back(); g_prof.pool.pop_back();
+        rec.b = g_prof.pool.back(); g_prof.pool.pop_back();
+        recorded = true;
+      } else {
+        g_prof.extra[stage]++;
+      }
+    }
+  }
+  if (recorded) cudaEventRecord(rec.a, st);
+  const cudaError_t e = f();
+  if (recorded) {
+    cudaEventRecord(rec.b, st);
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    g_prof.recs.push_back(rec);
+  }
+  if (e == cudaSuccess) g_launches.fetch_add(1);
+  return e;
+}
+
+// ------------------------------------------------------------------ workspace plan
+constexpr size_t kAlign = 256;
+size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Plan {
+  int n_split = 1, split_len = 0;
+  size_t off_scores = 0, off_topk = 0, off_po = 0, off_pml = 0, off_tc = 0, total = 0;
+};
+
+Plan make_plan(const csa_config* c, int B, int S, int64_t n_cap) {
+  Plan p;
+  const bool hca = c->top_k == 0;
+  const int64_t c_max = (int64_t)c->window + (hca ? n_cap : c->top_k);
+  if (S == 1) {                               // decode: split the candidates across CTAs
+    p.split_len = use_tc(c) ? tc_attn_split_len() : 64;
+    p.n_split = (int)((c_max + p.split_len - 1) / p.split_len);
+    if (p.n_split < 1) p.n_split = 1;
+  } else {
+    p.split_len = (int)c_max;
+    p.n_split = 1;
+  }
+  size_t o = 0;
+  const size_t rows = (size_t)B * (size_t)S;
+  if (!hca) {
+    p.off_scores = o; o = up(o + rows * (size_t)n_cap * sizeof(float));
+    p.off_topk = o;   o = up(o + rows * (size_t)c->top_k * sizeof(int32_t));
+  }
+  if (p.n_split > 1) {
+    p.off_po = o;  o = up(o + rows * p.n_split * (size_t)c->H * c->d * sizeof(float));
+    p.off_pml = o; o = up(o + rows * p.n_split * (size_t)c->H * 2 * sizeof(float));
+  }
+  p.off_tc = o;
+  o = up(o + tc_workspace_bytes(B, S, n_cap, c->top_k));
+  p.total = o;
+  return p;
+}
+
+template <typename T>
+T* carve(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+csa_status check_ws(const Plan& pl, void* ws, size_t ws_bytes) {
+  if (ws_bytes < pl.total) return fail(CSA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes, pl.total);
+  if (pl.total && !ws) return fail(CSA_ERR_INVALID_ARG, "ws is NULL");
+  if (ws && !aligned16(ws)) return fail(CSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+  return CSA_OK;
+}
+
+// ------------------------------------------------------------------ stage launchers
+csa_status run_compress(const csa_config* c, int B, const csa_cache* k, int64_t first, int64_t n,
+                        const int64_t* pos, cudaStream_t st) {
+  CompressParams p;
+  memset(&p, 0, sizeof p);
+  p.job[0] = CompressJob{k->kv, k->gate, k->gate_bias, k->ckv, c->d};
+  p.n_jobs = 1;
+  if (c->top_k > 0 && k->idx_k) {
+    p.job[1] = CompressJob{k->idx_k, k->idx_gate, k->idx_bias, k->cidx, c->d_idx};
+    p.n_jobs = 2;
+  }
+  p.N = k->N; p.n_cap = k->n_cap; p.first_entry = first; p.n_entries = n; p.pos = pos;
+  p.ratio = c->ratio; p.eps = c->rms_eps; p.rope = make_rope(c); p.err = device_error_word();
+  return cuda_status(launch_stage(ST_COMPRESS, st, [&] { return launch_compress(c->storage == CSA_BF16, B, p, st); }),
+                     "compress launch");
+}
+
+csa_status run_index_topk(const csa_config* c, int B, int S, const int64_t* pos, const void* q_idx,
+                          const float* w, const void* cidx, int64_t n_cap, int32_t* topk,
+                          float* scores, void* tc_ws, cudaStream_t st) {
+  const bool bf16 = c->storage == CSA_BF16;
+  if (use_tc(c)) {
+    const RopeTab rope = make_rope(c);
+    int32_t* err = device_error_word();
+    cudaError_t e = launch_stage(ST_INDEX, st, [&] {
+      return tc_index_scores(B, S, pos, q_idx, w, cidx, n_cap, c->ratio, rope, scores, tc_ws, err, st);
+    });
+    if (e != cudaSuccess) return cuda_status(e, "tcgen05 indexer launch");
+  } else {
+    IndexParams ip;
+    memset(&ip, 0, sizeof ip);
+    ip.q_idx = q_idx; ip.w = w; ip.cidx = cidx; ip.scores = scores; ip.pos = pos; ip.n_cap = n_cap;
+    ip.S = S; ip.H_idx = c->H_idx; ip.ratio = c->ratio; ip.rope = make_rope(c);
+    csa_status s = cuda_status(launch_stage(ST_INDEX, st, [&] { return launch_index_simt(bf16, B, ip, st); }),
+                               "indexer launch");
+    if (s != CSA_OK) return s;
+  }
+  TopkParams tp;
+  tp.scores = scores; tp.topk = topk; tp.pos = pos; tp.n_cap = n_cap; tp.S = S; tp.k = c->top_k;
+  tp.ratio = c->ratio;
+  return cuda_status(launch_stage(ST_TOPK, st, [&] { return launch_topk(B, tp, st); }), "top-k launch");
+}
+
+csa_status run_attn(const csa_config* c, const Plan& pl, int B, int S, const int64_t* pos,
+                    const void* q, const void* kv, int64_t N, const void* ckv, int64_t n_cap,
+                    const int32_t* topk, const float* sink, void* out, void* ws, cudaStream_t st) {
+  AttnParams ap;
+  memset(&ap, 0, sizeof ap);
+  ap.q = q; ap.kv = kv; ap.ckv = ckv; ap.topk = c->top_k > 0 ? topk : nullptr; ap.sink = sink;
+  ap.out = out; ap.pos = pos; ap.N = N; ap.n_cap = n_cap; ap.S = S; ap.H = c->H; ap.k = c->top_k;
+  ap.ratio = c->ratio; ap.window = c->window; ap.n_split = pl.n_split; ap.split_len = pl.split_len;
+  ap.scale = softmax_scale(c); ap.rope = make_rope(c); ap.err = device_error_word();
+  if (pl.n_split > 1) { ap.part_o = carve<float>(ws, pl.off_po); ap.part_ml = carve<float>(ws, pl.off_pml); }
+  const bool bf16 = c->storage == CSA_BF16;
+  cudaError_t e;
+  if (use_tc(c)) e = launch_stage(ST_ATTN, st, [&] { return tc_sparse_attn(B, ap, carve<char>(ws, pl.off_tc), st); });
+  else e = launch_stage(ST_ATTN, st, [&] { return launch_attn_simt(bf16, B, ap, st); });
+  if (e != cudaSuccess) return cuda_status(e, "attention launch");
+  if (pl.n_split <= 1) return CSA_OK;
+  return cuda_status(launch_stage(ST_MERGE, st, [&] { return launch_attn_merge(bf16, B, ap, st); }), "merge launch");
+}
+
+csa_status check_cache_ptrs(const csa_config* c, const csa_cache* k, bool need_idx) {
+  if (!k) return fail(CSA_ERR_INVALID_ARG, "cache is NULL");
+  CHECK_PTR(k->kv); CHECK_PTR(k->gate); CHECK_PTR(k->gate_bias); CHECK_PTR(k->ckv);
+  if (need_idx) { CHECK_PTR(k->idx_k); CHECK_PTR(k->idx_gate); CHECK_PTR(k->idx_bias); CHECK_PTR(k->cidx); }
+  if (k->N < 1 || k->n_cap < 1) return fail(CSA_ERR_SHAPE, "cache N = %lld, n_cap = %lld", (long long)k->N, (long long)k->n_cap);
+  (void)c;
+  return CSA_OK;
+}
+
+}  // namespace
+
+// ================================================================== C ABI
+extern "C" {
+
+const char* csa_status_string(csa_status s) {
+  switch (s) {
+    case CSA_OK: return "ok";
+    case CSA_ERR_INVALID_ARG: return "invalid argument";
+    case CSA_ERR_SHAPE: return "unsupported or inconsistent shape";
+    case CSA_ERR_DTYPE: return "unsupported dtype";
+    case CSA_ERR_WORKSPACE: return "workspace too small";
+    case CSA_ERR_CUDA: return "CUDA error";
+    case CSA_ERR_DEVICE: return "device-side error";
+    case CSA_ERR_NOT_IMPLEMENTED: return "not implemented";
+  }
+  return "unknown status";
+}
+
+const char* csa_last_error(void) { return g_last_error.c_str(); }
+
+csa_status csa_get_device_status(cudaStream_t stream, int reset, int32_t* code) {
+  int32_t* w = device_error_word();
+  if (!w) return fail(CSA_ERR_CUDA, "device error word unavailable");
+  csa_status s = cuda_status(cudaStreamSynchronize(stream), "stream synchronize");
+  if (s != CSA_OK) return s;
+  int32_t v = 0;
+  s = cuda_status(cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost), "read error word");
+  if (s != CSA_OK) return s;
+  if (reset) {
+    s = cuda_status(cudaMemset(w, 0, sizeof v), "clear error word");
+    if (s != CSA_OK) return s;
+    s = cuda_status(cudaDeviceSynchronize(), "clear error word");
+    if (s != CSA_OK) return s;
+  }
+  if (code) *code = v;
+  return v ? CSA_ERR_DEVICE : CSA_OK;
+}
+
+size_t csa_workspace_bytes(const csa_config* cfg, int32_t B, int32_t S, int64_t n_cap) {
+  if (check_config(cfg) != CSA_OK || B < 0 || S < 0 || n_cap < 0) return 0;
+  return make_plan(cfg, B, S, n_cap).total;
+}
+
+csa_status csa_compress(const csa_config* cfg, int32_t B, const csa_cache* cache, int64_t first_entry,
+                        int64_t n_entries, cudaStream_t stream) {
+  csa_status s = check_config(cfg);
+  if (s != CSA_OK) return s;
+  if (B < 0 || B > 65535) return fail(CSA_ERR_SHAPE, "B = %d", B);
+  s = check_cache_ptrs(cfg, cache, cfg->top_k > 0 && cache && cache->idx_k);
+  if (s != CSA_OK) return s;
+  if (first_entry < 0 || n_entries < 0) return fail(CSA_ERR_INVALID_ARG, "negative entry range");
+  if ((first_entry + n_entries) * cfg->ratio > cache->N)
+    return fail(CSA_ERR_SHAPE, "entries up to %lld need %lld raw tokens > N = %lld",
+                (long long)(first_entry + n_entries), (long long)((first_entry + n_entries) * cfg->ratio),
+                (long long)cache->N);
+  if (first_entry + n_entries > cache->n_cap) return fail(CSA_ERR_SHAPE, "entry range exceeds n_cap");
+  if (B == 0 || n_entries == 0) return CSA_OK;
+  return run_compress(cfg, B, cache, first_entry, n_entries, nullptr, stream);
+}
+
+csa_status csa_index_topk(const csa_config* cfg, int32_t B, int32_t S, const int64_t* pos,
+                          const void* q_idx, const float* w, const void* cidx, int64_t n_cap,
+                          int32_t* topk, float* scores, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  csa_status s = check_config(cfg);
+  if (s != CSA_OK) return s;
+  if (cfg->top_k == 0) return fail(CSA_ERR_INVALID_ARG, "top_k == 0 (HCA) has no indexer");
+  if (B < 0 || B > 65535 || S < 0 || S > 65535) return fail(CSA_ERR_SHAPE, "B = %d, S = %d", B, S);
+  if (n_cap < 1) return fail(CSA_ERR_SHAPE, "n_cap = %lld", (long long)n_cap);
+  CHECK_PTR(pos); CHECK_PTR(q_idx); CHECK_PTR(w); CHECK_PTR(cidx); CHECK_PTR(topk); CHECK_OPT_PTR(scores);
+  const Plan pl = make_plan(cfg, B, S, n_cap);
+  s = check_ws(pl, ws, ws_bytes);
+  if (s != CSA_OK) return s;
+  if (B == 0 || S == 0) return CSA_OK;
+  float* sc = scores ? scores : carve<float>(ws, pl.off_scores);
+  return run_index_topk(cfg, B, S, pos, q_idx, w, cidx, n_cap, topk, sc, carve<char>(ws, pl.off_tc), stream);
+}
+
+csa_status csa_sparse_attn(const csa_config* cfg, int32_t B, int32_t S, const int64_t* pos, const void* q,
+                           const void* kv, int64_t N, const void* ckv, int64_t n_cap, const int32_t* topk,
+                           const float* sink, void* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  csa_status s = check_config(cfg);
+  if (s != CSA_OK) return s;
+  if (B < 0 || B > 65535 || S < 0 || S > 65535) return fail(CSA_ERR_SHAPE, "B = %d, S = %d", B, S);
+  if (N < 1 || n_cap < 1) return fail(CSA_ERR_SHAPE, "N = %lld, n_cap = %lld", (long long)N, (long long)n_cap);
+  CHECK_PTR(pos); CHECK_PTR(q); CHECK_PTR(kv); CHECK_PTR(ckv); CHECK_PTR(sink); CHECK_PTR(out);
+  if (cfg->top_k > 0) CHECK_PTR(topk);
+  const Plan pl = make_plan(cfg, B, S, n_cap);
+  s = check_ws(pl, ws, ws_bytes);
+  if (s != CSA_OK) return s;
+  if (B == 0 || S == 0) return CSA_OK;
+  return run_attn(cfg, pl, B, S, pos, q, kv, N, ckv, n_cap, topk, sink, out, ws, stream);
+}
+
+csa_status csa_decode(const csa_config* cfg, int32_t B, const int64_t* pos, const csa_cache* cache,
+                      const void* q, const void* q_idx, const float* w, const float* sink, void* out,
+                      int32_t* topk_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  csa_status s = check_config(cfg);
+  if (s != CSA_OK) return s;
+  const bool hca = cfg->top_k == 0;
+  if (B < 0 || B > 65535) return fail(CSA_ERR_SHAPE, "B = %d", B);
+  s = check_cache_ptrs(cfg, cache, !hca);
+  if (s != CSA_OK) return s;
+  CHECK_PTR(pos); CHECK_PTR(q); CHECK_PTR(sink); CHECK_PTR(out); CHECK_OPT_PTR(topk_out);
+  if (!hca) { CHECK_PTR(q_idx); CHECK_PTR(w); }
+  const Plan pl = make_plan(cfg, B, 1, cache->n_cap);
+  s = check_ws(pl, ws, ws_bytes);
+  if (s != CSA_OK) return s;
+  if (B == 0) return CSA_OK;
+  s = run_compress(cfg, B, cache, 0, 0, pos, stream);
+  if (s != CSA_OK) return s;
+  int32_t* tk = nullptr;
+  if (!hca) {
+    tk = topk_out ? topk_out : carve<int32_t>(ws, pl.off_topk);
+    s = run_index_topk(cfg, B, 1, pos, q_idx, w, cache->cidx, cache->n_cap, tk,
+                       carve<float>(ws, pl.off_scores), carve<char>(ws, pl.off_tc), stream);
+    if (s != CSA_OK) return s;
+  }
+  return run_attn(cfg, pl, B, 1, pos, q, cache->kv, cache->N, cache->ckv, cache->n_cap, tk, sink, out, ws,
+                  stream);
+}
+
+csa_status csa_prefill(const csa_config* cfg, int32_t B, int32_t S, const csa_cache* cache, const void* q,
+                       const void* q_idx, const float* w, const float* sink, void* out, int32_t* topk_out,
+                       void* ws, size_t ws_bytes, cudaStream_t stream) {
+  csa_status s = check_config(cfg);
+  if (s != CSA_OK) return s;
+  const bool hca = cfg->top_k == 0;
+  if (B < 0 || B > 65535 || S < 0 || S > 65535) return fail(CSA_ERR_SHAPE, "B = %d, S = %d", B, S);
+  s = check_cache_ptrs(cfg, cache, !hca);
+  if (s != CSA_OK) return s;
+  if (S > cache->N) return fail(CSA_ERR_SHAPE, "S = %d > N = %lld", S, (long long)cache->N);
+  if (S / cfg->ratio > cache->n_cap) return fail(CSA_ERR_SHAPE, "S / ratio entries exceed n_cap");
+  CHECK_PTR(q); CHECK_PTR(sink); CHECK_PTR(out); CHECK_OPT_PTR(topk_out);
+  if (!hca) { CHECK_PTR(q_idx); CHECK_PTR(w); }
+  const Plan pl = make_plan(cfg, B, S, cache->n_cap);
+  s = check_ws(pl, ws, ws_bytes);
+  if (s != CSA_OK) return s;
+  if (B == 0 || S == 0) return CSA_OK;
+  s = run_compress(cfg, B, cache, 0, S / cfg->ratio, nullptr, stream);
+  if (s != CSA_OK) return s;
+  int32_t* tk = nullptr;
+  if (!hca) {
+    tk = topk_out ? topk_out : carve<int32_t>(ws, pl.off_topk);
+    s = run_index_topk(cfg, B, S, nullptr, q_idx, w, cache->cidx, cache->n_cap, tk,
+                       carve<float>(ws, pl.off_scores), carve<char>(ws, pl.off_tc), stream);
+    if (s != CSA_OK) return s;
+  }
+  return run_attn(cfg, pl, B, S, nullptr, q, cache->kv, cache->N, cache->ckv, cache->n_cap, tk, sink, out,
+                  ws, stream);
+}
+
+int64_t csa_launch_count(void) { return g_launches.load(); }
+
+csa_status csa_profile_begin(int32_t max_launches) {
+  if (max_launches < 0) return fail(CSA_ERR_INVALID_ARG, "max_launches < 0");
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  for (auto& r : g_prof.recs) { g_prof.pool.push_back(r.a); g_prof.pool.push_back(r.b); }
+  g_prof.recs.clear();
+  for (int s = 0; s < ST_COUNT; ++s) g_prof.extra[s] = 0;
+  while ((int)g_prof.pool.size() < 2 * max_launches) {
+    cudaEvent_t ev;
+    if (cudaEventCreate(&ev) != cudaSuccess) return fail(CSA_ERR_CUDA, "cudaEventCreate failed");
+    g_prof.pool.push_back(ev);
+  }
+  g_prof.cap = max_launches;
+  g_prof.recs.reserve(max_launches);
+  g_prof.on = true;
+  return CSA_OK;
+}
+
+csa_status csa_profile_end(float* ms, int32_t* launches, int32_t n_stages) {
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  g_prof.on = false;
+  for (int s = 0; s < n_stages; ++s) {
+    if (ms) ms[s] = 0.f;
+    if (launches) launches[s] = s < ST_COUNT ? g_prof.extra[s] : 0;
+  }
+  csa_status st = CSA_OK;
+  for (auto& r : g_prof.recs) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) { st = fail(CSA_ERR_CUDA, "event synchronize failed"); continue; }
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) { st = fail(CSA_ERR_CUDA, "event elapsed failed"); continue; }
+    if (r.stage < n_stages) {
+      if (ms) ms[r.stage] += t;
+      if (launches) launches[r.stage] += 1;
+    }
+  }
+  return st;
+}
+
+}  // extern "C"

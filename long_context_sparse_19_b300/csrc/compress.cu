@@ -1,0 +1,172 @@
+// K1: the compressor — overlapped per-channel softmax pooling, RMSNorm, partial RoPE.
+//
+// [FLASH] "DeepSeek-V4-Flash 架构：一个 token 的旅程", sections "压缩是逐通道的 learned pooling"
+// (every channel runs its own softmax along the token axis; RMSNorm after pooling; RoPE on the last
+// 64 dims) and "一个通道，逐项算出压缩结果" (the first group has no previous group: its rows take
+// gate -inf, weight 0). Entry i pools tokens [(i-1)m, (i+1)m) with gate bias row p = j - (i-1)m.
+//
+// Design: a team of C/8 threads owns one request's run of consecutive entries; each thread owns
+// 8 adjacent channels and loads 16-byte vectors, so a team reads each raw row fully coalesced.
+// Each raw group g is read ONCE: its tokens update two online-softmax states at the same time,
+// one with the second-half bias rows (for entry g) and one with the first-half bias rows (for
+// entry g+1). An entry is the merge of the two states, which are exact softmax partials.
+#include "kernels.h"
+
+namespace csa {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kEntriesPerBlock = 64;
+
+struct Stat8 {
+  float mx[8], sum[8], acc[8];
+  __device__ __forceinline__ void clear() {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) { mx[k] = -INFINITY; sum[k] = 0.f; acc[k] = 0.f; }
+  }
+  __device__ __forceinline__ void add(int k, float l, float v) {
+    if (l > mx[k]) {
+      const float sc = expf(mx[k] - l);       // exp(-inf) = 0 on the first token
+      sum[k] = sum[k] * sc + 1.f;
+      acc[k] = acc[k] * sc + v;
+      mx[k] = l;
+    } else {
+      const float e = expf(l - mx[k]);
+      sum[k] += e;
+      acc[k] = fmaf(e, v, acc[k]);
+    }
+  }
+};
+
+// Reads group g (tokens g*m .. g*m+m-1) once; updates `lo` with bias rows [0, m) and, when
+// `want_hi`, `hi` with bias rows [m, 2m).
+template <typename T, int C>
+__device__ __forceinline__ void scan_group(const T* src, const T* gate, const float* bias, int64_t g,
+                                           int m, int c0, Stat8& lo, Stat8& hi, bool want_hi) {
+  for (int r = 0; r < m; ++r) {
+    const int64_t j = g * m + r;
+    float v[8], gt[8], bl[8], bh[8];
+    load8(src + j * C + c0, v);
+    load8(gate + j * C + c0, gt);
+    load8(bias + (int64_t)r * C + c0, bl);
+    if (want_hi) load8(bias + (int64_t)(m + r) * C + c0, bh);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      lo.add(k, gt[k] + bl[k], v[k]);
+      if (want_hi) hi.add(k, gt[k] + bh[k], v[k]);
+    }
+  }
+}
+
+template <typename T, int C>
+__device__ void compress_run(const CompressParams& p, const CompressJob& job, int b, int64_t e_begin,
+                             int64_t e_end, int team, int tt, float* red) {
+  constexpr int TPE = C / 8;               // threads per entry team
+  const int m = p.ratio;
+  const int c0 = tt * 8;
+  const T* src = reinterpret_cast<const T*>(job.src) + (int64_t)b * p.N * C;
+  const T* gate = reinterpret_cast<const T*>(job.gate) + (int64_t)b * p.N * C;
+  T* dst = reinterpret_cast<T*>(job.dst) + (int64_t)b * p.n_cap * C;
+  const int lane = threadIdx.x & 31;
+
+  Stat8 prev, lo, hi;
+  prev.clear();
+  if (e_begin >= 1) scan_group<T, C>(src, gate, job.bias, e_begin - 1, m, c0, prev, hi, false);
+
+  for (int64_t e = e_begin; e < e_end; ++e) {
+    lo.clear();
+    hi.clear();
+    scan_group<T, C>(src, gate, job.bias, e, m, c0, lo, hi, true);
+    float x[8];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float M = fmaxf(prev.mx[k], hi.mx[k]);
+      const float a = (prev.mx[k] == -INFINITY) ? 0.f : expf(prev.mx[k] - M);
+      const float bb = expf(hi.mx[k] - M);
+      x[k] = (prev.acc[k] * a + hi.acc[k] * bb) / (prev.sum[k] * a + hi.sum[k] * bb);
+      ss = fmaf(x[k], x[k], ss);
+      prev.mx[k] = lo.mx[k]; prev.sum[k] = lo.sum[k]; prev.acc[k] = lo.acc[k];
+    }
+    // RMSNorm over the C channels of the entry: reduce within the team.
+    if constexpr (TPE >= 32) {
+      ss = warp_sum(ss);
+      if constexpr (TPE > 32) {
+        constexpr int W = TPE / 32;
+        const int wit = tt >> 5;
+        if (lane == 0) red[team * W + wit] = ss;
+        named_barrier(1 + team, TPE);
+        ss = 0.f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) ss += red[team * W + w];
+        named_barrier(1 + team, TPE);
+      }
+    } else {
+      const unsigned mask = ((1u << (TPE & 31)) - 1u) << (lane & ~(TPE - 1));
+#pragma unroll
+      for (int o = TPE / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(mask, ss, o);
+    }
+    const float inv = 1.0f / sqrtf(ss / (float)C + p.eps);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] *= inv;
+    // RoPE of the last d_rope channels at position e*m (interleaved pairs).
+    const int r0 = C - p.rope.d_rope;
+    if (c0 >= r0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float c, s;
+        rope_cs(e * m, p.rope.theta[(c0 - r0) / 2 + q], c, s);
+        const float a = x[2 * q], bq = x[2 * q + 1];
+        x[2 * q] = a * c - bq * s;
+        x[2 * q + 1] = a * s + bq * c;
+      }
+    }
+    store8(dst + e * C + c0, x);
+  }
+}
+
+template <typename T, int C>
+__device__ void compress_block(const CompressParams& p, const CompressJob& job, float* red) {
+  constexpr int TPE = C / 8;
+  constexpr int TEAMS = kThreads / TPE;
+  const int team = threadIdx.x / TPE;
+  const int tt = threadIdx.x % TPE;
+  const int b = blockIdx.y;
+  int64_t e_begin, e_end;
+  if (p.pos) {                                        // close mode: one entry per request
+    if (blockIdx.x != 0 || team != 0) return;
+    const int64_t t = p.pos[b];
+    if (t < 0 || t >= p.N) { if (tt == 0) set_error(p.err, DEVERR_BAD_POS); return; }
+    if ((t + 1) % p.ratio != 0) return;
+    e_begin = t / p.ratio;
+    if (e_begin >= p.n_cap) { if (tt == 0) set_error(p.err, DEVERR_BAD_POS); return; }
+    e_end = e_begin + 1;
+  } else {
+    constexpr int EPT = kEntriesPerBlock / TEAMS;
+    e_begin = p.first_entry + (int64_t)blockIdx.x * kEntriesPerBlock + (int64_t)team * EPT;
+    e_end = min(e_begin + EPT, p.first_entry + p.n_entries);
+    if (e_begin >= e_end) return;
+  }
+  compress_run<T, C>(p, job, b, e_begin, e_end, team, tt, red);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) compress_kernel(const CompressParams p) {
+  __shared__ float red[16];
+  const CompressJob& job = p.job[blockIdx.z];
+  if (job.C == 512) compress_block<T, 512>(p, job, red);
+  else compress_block<T, 128>(p, job, red);
+}
+
+}  // namespace
+
+cudaError_t launch_compress(bool bf16, int B, const CompressParams& p, cudaStream_t st) {
+  const int64_t nb = p.pos ? 1 : (p.n_entries + kEntriesPerBlock - 1) / kEntriesPerBlock;
+  if (nb == 0 || B == 0) return cudaSuccess;
+  dim3 grid((unsigned)nb, (unsigned)B, (unsigned)p.n_jobs);
+  if (bf16) compress_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(p);
+  else compress_kernel<float><<<grid, kThreads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

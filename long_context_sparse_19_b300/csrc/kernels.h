@@ -1,0 +1,77 @@
+// Internal launch interface of the CSA / HCA kernels (not part of the C ABI).
+#pragma once
+
+#include "common.cuh"
+
+namespace csa {
+
+// ------------------------------------------------------------------ K1 compressor
+struct CompressJob {
+  const void* src;       // [B, N, C] raw rows
+  const void* gate;      // [B, N, C] gate logits
+  const float* bias;     // [2m, C]
+  void* dst;             // [B, n_cap, C]
+  int C;                 // 512 (kv) or 128 (index keys)
+};
+
+struct CompressParams {
+  CompressJob job[2];    // job[1] used when n_jobs == 2
+  int n_jobs;
+  int64_t N, n_cap;
+  int64_t first_entry, n_entries;   // range mode
+  const int64_t* pos;    // close mode when non-null: entry pos[b]/m if (pos[b]+1) % m == 0
+  int ratio;
+  float eps;
+  RopeTab rope;
+  int32_t* err;
+};
+
+cudaError_t launch_compress(bool bf16, int B, const CompressParams& p, cudaStream_t st);
+
+// ------------------------------------------------------------------ K2 / K6 indexer scores (SIMT)
+struct IndexParams {
+  const void* q_idx;     // [B, S, H_idx, d_idx]
+  const float* w;        // [B, S, H_idx]
+  const void* cidx;      // [B, n_cap, d_idx]
+  float* scores;         // [B, S, n_cap]
+  const int64_t* pos;    // [B, S]; null: t = s
+  int64_t n_cap;
+  int S, H_idx, ratio;
+  RopeTab rope;
+};
+
+cudaError_t launch_index_simt(bool bf16, int B, const IndexParams& p, cudaStream_t st);
+
+// ------------------------------------------------------------------ K3 top-k
+struct TopkParams {
+  const float* scores;   // [B, S, n_cap]
+  int32_t* topk;         // [B, S, k]
+  const int64_t* pos;    // [B, S]; null: t = s
+  int64_t n_cap;
+  int S, k, ratio;
+};
+
+cudaError_t launch_topk(int B, const TopkParams& p, cudaStream_t st);
+
+// ------------------------------------------------------------------ K4 / K5 attention (SIMT)
+struct AttnParams {
+  const void* q;         // [B, S, H, d]
+  const void* kv;        // [B, N, d]
+  const void* ckv;       // [B, n_cap, d]
+  const int32_t* topk;   // [B, S, k] or null (HCA)
+  const float* sink;     // [H]
+  void* out;             // [B, S, H, d]
+  const int64_t* pos;    // [B, S]; null: t = s
+  float* part_o;         // [B, S, n_split, H, d]   (n_split > 1)
+  float* part_ml;        // [B, S, n_split, H, 2]
+  int64_t N, n_cap;
+  int S, H, k, ratio, window, n_split, split_len;
+  float scale;
+  RopeTab rope;
+  int32_t* err;
+};
+
+cudaError_t launch_attn_simt(bool bf16, int B, const AttnParams& p, cudaStream_t st);
+cudaError_t launch_attn_merge(bool bf16, int B, const AttnParams& p, cudaStream_t st);
+
+}  // namespace csa

@@ -1,0 +1,21 @@
+// tcgen05 (5th-generation tensor core) kernels of the bf16 path: indexer scores and the gathered
+// sparse attention. Dispatched by the C ABI for bf16 storage with H = 64 (and H_idx = 64).
+#pragma once
+
+#include "kernels.h"
+
+namespace csa {
+
+bool tc_enabled();                                            // false: the SIMT kernels run instead
+int tc_attn_split_len();                                      // candidates per attention CTA (decode)
+size_t tc_workspace_bytes(int B, int S, int64_t n_cap, int top_k);
+
+// s_i = sum_h w_h relu(rope(q_h, t) . cidx_i) for i < visible(t), bf16 operands, fp32 accumulate.
+cudaError_t tc_index_scores(int B, int S, const int64_t* pos, const void* q_idx, const float* w,
+                            const void* cidx, int64_t n_cap, int ratio, const RopeTab& rope,
+                            float* scores, void* ws, int32_t* err, cudaStream_t st);
+
+// Sparse attention (split partials when p.n_split > 1, else the final output).
+cudaError_t tc_sparse_attn(int B, const AttnParams& p, void* ws, cudaStream_t st);
+
+}  // namespace csa

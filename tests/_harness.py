@@ -1,0 +1,130 @@
+"""Shared test plumbing: seeded inputs on the device, the oracle on the same values, and the
+tolerance checks. Test infrastructure only (imports the oracle)."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import synth
+from oracle import csa_oracle as O
+
+# Tolerances (see the design notes): indexer |ds| <= 1e-3 * max(|s_ref|, rms_row(s_ref)); attention
+# max|do| / max|o_ref| per (request, query, head) <= 1e-2 for bf16 storage and 1e-5 for float32;
+# compressed entries are one bf16 rounding (2^-8 relative, i.e. one ulp) or 1e-5 for float32.
+ATTN_TOL = {"bf16": 1e-2, "f32": 1e-5}
+SCORE_TOL = {"bf16": 1e-3, "f32": 1e-5}
+TIE_TOL = 1e-4
+
+
+def lib():
+    import long_context_sparse_19_b300 as L
+    return L
+
+
+def configs(wl: synth.Workload, simt: bool = False):
+    L = lib()
+    c = L.Config(H=wl.H, d=wl.d, d_rope=wl.d_rope, H_idx=wl.H_idx, d_idx=wl.d_idx, ratio=wl.ratio,
+                 top_k=wl.top_k, window=wl.window, storage=wl.storage, simt=simt)
+    o = O.OracleConfig(H=wl.H, d=wl.d, d_rope=wl.d_rope, H_idx=wl.H_idx, d_idx=wl.d_idx, ratio=wl.ratio,
+                       top_k=wl.top_k, window=wl.window)
+    return c, o
+
+
+def dev(a: np.ndarray, storage: str, device="cuda") -> torch.Tensor:
+    """float32 host values (already representable in the storage type) -> device tensor."""
+    if storage == "bf16":
+        bits = synth.bf16_bits(a).view(np.int16)
+        return torch.from_numpy(bits).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
+
+
+def host64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+class DeviceBatch:
+    """Every tensor of a workload's B requests on the GPU, plus the host copies the oracle reads."""
+
+    def __init__(self, wl: synth.Workload, requests=None, device="cuda"):
+        self.wl = wl
+        self.reqs = synth.gen_requests(wl, requests)
+        self.shared = synth.gen_shared(wl)
+        st = wl.storage
+        stack = lambda k: np.stack([r[k] for r in self.reqs])
+        self.kv = dev(stack("kv"), st)
+        self.gate = dev(stack("gate"), st)
+        self.bias = torch.from_numpy(self.shared["bias"]).to(device)
+        self.sink = torch.from_numpy(self.shared["sink"]).to(device)
+        self.q = dev(stack("q"), st)
+        B = len(self.reqs)
+        n_cap = wl.n_entries
+        dt = torch.bfloat16 if st == "bf16" else torch.float32
+        self.ckv = torch.full((B, n_cap, wl.d), float("nan"), dtype=dt, device=device)
+        if wl.hca:
+            self.idx_k = self.idx_gate = self.idx_bias = self.cidx = self.q_idx = self.w = None
+        else:
+            self.idx_k = dev(stack("idx_k"), st)
+            self.idx_gate = dev(stack("idx_gate"), st)
+            self.idx_bias = torch.from_numpy(self.shared["idx_bias"]).to(device)
+            self.cidx = torch.full((B, n_cap, wl.d_idx), float("nan"), dtype=dt, device=device)
+            self.q_idx = dev(stack("q_idx"), st)
+            self.w = torch.from_numpy(stack("w")).to(device)
+
+    @property
+    def B(self):
+        return len(self.reqs)
+
+    def cache(self):
+        L = lib()
+        return L.Cache(kv=self.kv, gate=self.gate, gate_bias=self.bias, ckv=self.ckv, idx_k=self.idx_k,
+                       idx_gate=self.idx_gate, idx_bias=self.idx_bias, cidx=self.cidx)
+
+
+# ------------------------------------------------------------------------------------ checks
+def check_entries(got: np.ndarray, ref: np.ndarray, storage: str, what: str):
+    if storage == "bf16":
+        bad = np.abs(got - ref) > 2.0 ** -8 * np.abs(ref) + 1e-6
+    else:
+        bad = np.abs(got - ref) > 1e-5 * np.maximum(1.0, np.abs(ref))
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} elements off; max err " \
+                          f"{np.abs(got - ref).max():.3g}"
+
+
+def check_scores(got: np.ndarray, ref: np.ndarray, storage: str, what: str):
+    scale = max(np.sqrt(np.mean(ref * ref)), 1e-30)
+    err = np.abs(got - ref) / np.maximum(np.abs(ref), scale)
+    assert err.max() <= SCORE_TOL[storage], f"{what}: max relative score error {err.max():.3g}"
+
+
+def check_topk_exact(got: np.ndarray, scores: np.ndarray, k: int, what: str):
+    """The GPU selection equals the exact selection on the same float32 scores."""
+    want = O.topk_select(scores, k)
+    assert np.array_equal(got, want), f"{what}: top-k differs from the exact selection on its scores"
+
+
+def check_topk_vs_oracle(got: np.ndarray, ref_scores: np.ndarray, k: int, what: str):
+    """Set equality with the oracle's selection, except swaps among entries whose oracle scores lie
+    within TIE_TOL * |s_k| of the k-th score."""
+    want = O.topk_select(ref_scores, k)
+    g = set(int(i) for i in got if i >= 0)
+    w = set(int(i) for i in want if i >= 0)
+    assert len(g) == len(w), f"{what}: {len(g)} selected, oracle {len(w)}"
+    if g == w:
+        return
+    sk = ref_scores[want[min(k, len(w)) - 1]]
+    band = TIE_TOL * max(abs(sk), 1e-30)
+    for i in g ^ w:
+        assert abs(ref_scores[i] - sk) <= band, \
+            f"{what}: entry {i} (score {ref_scores[i]:.6g}) differs from the oracle selection beyond " \
+            f"the tie band around s_k = {sk:.6g}"
+
+
+def check_attn(got: np.ndarray, ref: np.ndarray, storage: str, what: str):
+    """got/ref: [H, d] for one query."""
+    num = np.abs(got - ref).max(axis=1)
+    den = np.maximum(np.abs(ref).max(axis=1), 1e-30)
+    rel = num / den
+    assert rel.max() <= ATTN_TOL[storage], f"{what}: max relative attention error {rel.max():.3g} " \
+                                           f"(head {int(rel.argmax())})"
