@@ -95,9 +95,14 @@ float softmax_scale(const csa_config* c) {
   return c->softmax_scale > 0.f ? c->softmax_scale : (float)(1.0 / sqrt((double)c->d));
 }
 
-bool use_tc(const csa_config* c) {
-  return tc_enabled() && c->storage == CSA_BF16 && !(c->flags & CSA_FLAG_SIMT) && c->H == 64 &&
-         (c->top_k == 0 || c->H_idx == 64);
+bool use_tc_index(const csa_config* c) {
+  return tc_index_available() && c->storage == CSA_BF16 && !(c->flags & CSA_FLAG_SIMT) && c->top_k > 0 &&
+         c->H_idx == 64 && c->d_idx == 128;
+}
+
+bool use_tc_attn(const csa_config* c) {
+  return tc_attn_available() && c->storage == CSA_BF16 && !(c->flags & CSA_FLAG_SIMT) && c->H == 64 &&
+         c->d == 512;
 }
 
 // ------------------------------------------------------------------ launch counting / stage profiling
@@ -161,7 +166,7 @@ Plan make_plan(const csa_config* c, int B, int S, int64_t n_cap) {
   const bool hca = c->top_k == 0;
   const int64_t c_max = (int64_t)c->window + (hca ? n_cap : c->top_k);
   if (S == 1) {                               // decode: split the candidates across CTAs
-    p.split_len = use_tc(c) ? tc_attn_split_len() : 64;
+    p.split_len = use_tc_attn(c) ? tc_attn_split_len() : 64;
     p.n_split = (int)((c_max + p.split_len - 1) / p.split_len);
     if (p.n_split < 1) p.n_split = 1;
   } else {
@@ -215,7 +220,7 @@ csa_status run_index_topk(const csa_config* c, int B, int S, const int64_t* pos,
                           const float* w, const void* cidx, int64_t n_cap, int32_t* topk,
                           float* scores, void* tc_ws, cudaStream_t st) {
   const bool bf16 = c->storage == CSA_BF16;
-  if (use_tc(c)) {
+  if (use_tc_index(c)) {
     const RopeTab rope = make_rope(c);
     int32_t* err = device_error_word();
     cudaError_t e = launch_stage(ST_INDEX, st, [&] {
@@ -249,7 +254,7 @@ csa_status run_attn(const csa_config* c, const Plan& pl, int B, int S, const int
   if (pl.n_split > 1) { ap.part_o = carve<float>(ws, pl.off_po); ap.part_ml = carve<float>(ws, pl.off_pml); }
   const bool bf16 = c->storage == CSA_BF16;
   cudaError_t e;
-  if (use_tc(c)) e = launch_stage(ST_ATTN, st, [&] { return tc_sparse_attn(B, ap, carve<char>(ws, pl.off_tc), st); });
+  if (use_tc_attn(c)) e = launch_stage(ST_ATTN, st, [&] { return tc_sparse_attn(B, ap, carve<char>(ws, pl.off_tc), st); });
   else e = launch_stage(ST_ATTN, st, [&] { return launch_attn_simt(bf16, B, ap, st); });
   if (e != cudaSuccess) return cuda_status(e, "attention launch");
   if (pl.n_split <= 1) return CSA_OK;
