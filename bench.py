@@ -219,10 +219,12 @@ def make_cache(T, wl, device):
 
 # ----------------------------------------------------------------------------- our decode leg
 def run_decode(args, world, rank, device, peaks) -> dict:
+    import dataclasses
     import torch
     import long_context_sparse_19_b300 as L
-    wl = DECODE_WL
+    wl = dataclasses.replace(DECODE_WL, B=args.B) if args.B else DECODE_WL
     B = wl.B
+    R = args.rotations
     cfg = make_cfg(wl)
     t_setup = time.time()
     T = device_inputs(wl, list(range(rank * B, rank * B + B)), device)
@@ -230,7 +232,7 @@ def run_decode(args, world, rank, device, peaks) -> dict:
     L.csa_compress(cfg, cache, 0, wl.n_entries)            # the caches the decode step reads
     pos = torch.full((B,), wl.t, dtype=torch.int64, device=device)
     rot = []
-    for r in range(ROTATIONS):
+    for r in range(R):
         if r == 0:
             c, q, qi, w = cache, T["q"][:, 0].contiguous(), T["q_idx"][:, 0].contiguous(), T["w"][:, 0].contiguous()
         else:
@@ -256,11 +258,11 @@ def run_decode(args, world, rank, device, peaks) -> dict:
         with torch.cuda.graph(g):
             r["call"]()
         graphs.append(g)
-    launches_per_step = (L.csa_launch_count() - n0) // ROTATIONS
+    launches_per_step = (L.csa_launch_count() - n0) // R
     assert L.csa_get_device_status() == 0
 
     for i in range(args.warmup):
-        graphs[i % ROTATIONS].replay()
+        graphs[i % R].replay()
     K = args.steps
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(gpu_ident(device))
@@ -270,7 +272,7 @@ def run_decode(args, world, rank, device, peaks) -> dict:
     wall0 = time.time()
     ev0.record()
     for i in range(K):
-        graphs[i % ROTATIONS].replay()
+        graphs[i % R].replay()
     ev1.record()
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -286,7 +288,7 @@ def run_decode(args, world, rank, device, peaks) -> dict:
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for i in range(K):
-        rot[i % ROTATIONS]["call"]()
+        rot[i % R]["call"]()
     e1.record()
     torch.cuda.synchronize()
     prof = L.csa_profile_end()
@@ -294,7 +296,7 @@ def run_decode(args, world, rank, device, peaks) -> dict:
 
     # End to end: per step, the step's inputs (q, q_idx, w, the new token's raw rows) come from
     # pinned host memory and the output goes back to pinned host memory, all inside the region.
-    e2e = run_e2e(args, wl, rot, world, device)
+    e2e = None if args.no_e2e else run_e2e(args, wl, rot, world, device)
     assert L.csa_get_device_status() == 0
 
     work = decode_work(wl, B)
@@ -346,8 +348,10 @@ def run_e2e(args, wl, rot, world, device) -> dict:
               for k in ("q", "q_idx", "w", "pos", "kv", "gate", "idx_k", "idx_gate"))
     d2h = host[0]["out"].numel() * host[0]["out"].element_size()
 
+    R = len(rot)
+
     def step(i):
-        r, hb = rot[i % ROTATIONS], host[i % ROTATIONS]
+        r, hb = rot[i % R], host[i % R]
         c = r["cache"]
         r["q"].copy_(hb["q"], non_blocking=True)
         r["q_idx"].copy_(hb["q_idx"], non_blocking=True)
@@ -511,12 +515,14 @@ def run_reference(args, world, rank) -> None:
 METRIC = "CSA decode query-tokens/s (N=65,536, B=32, H=64, top-k 512, W=128, bf16)"
 
 
-def decode_config(world) -> dict:
+def decode_config(world, args=None) -> dict:
     wl = DECODE_WL
-    return {"workload": wl.name, "B_per_gpu": wl.B, "N": wl.N, "t": wl.t, "H": wl.H, "H_idx": wl.H_idx,
+    R = args.rotations if args else ROTATIONS
+    B = args.B if args and args.B else wl.B
+    return {"workload": wl.name, "B_per_gpu": B, "N": wl.N, "t": wl.t, "H": wl.H, "H_idx": wl.H_idx,
             "top_k": wl.top_k, "window": wl.window, "ratio": wl.ratio, "parallelism": f"requests x{world}",
-            "l2": f"inputs rotated over {ROTATIONS} device copies (~{ROTATIONS * 153} MB touched per cycle "
-                  f"> 126 MB L2)", "timing": "CUDA graph of one csa_decode call per step, CUDA events"}
+            "l2": f"inputs rotated over {R} device copies (~{R * 153 * B // 32} MB touched per cycle; "
+                  f"L2 is 126 MB)", "timing": "CUDA graph of one csa_decode call per step, CUDA events"}
 
 
 def main():
@@ -529,6 +535,9 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--B", type=int, default=0, help="requests per GPU (default: the workload's 32)")
+    ap.add_argument("--rotations", type=int, default=ROTATIONS, help="device input copies cycled between steps")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -553,7 +562,7 @@ def main():
         line = {"metric": METRIC, "value": dec["value"], "unit": "query-tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": dec["ms_per_step"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-                "data": "synthetic", "config": decode_config(world),
+                "data": "synthetic", "config": decode_config(world, args),
                 "hbm_gbs": dec["hbm_gbs"], "hbm_frac_of_measured": dec["hbm_frac_of_measured"],
                 "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
                 "gpu_launches": dec["gpu_launches"], "clocks": dec["clocks"],

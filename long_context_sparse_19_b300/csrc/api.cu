@@ -87,7 +87,12 @@ RopeTab make_rope(const csa_config* c) {
   RopeTab r;
   memset(&r, 0, sizeof r);
   r.d_rope = c->d_rope;
-  for (int i = 0; i < c->d_rope / 2; ++i) r.theta[i] = pow((double)c->rope_base, -2.0 * i / c->d_rope);
+  const double inv_pi = 0.31830988618379067153776752674503;
+  for (int i = 0; i < c->d_rope / 2; ++i) {
+    const double tp = pow((double)c->rope_base, -2.0 * i / c->d_rope) * inv_pi;
+    r.th_hi[i] = (float)tp;
+    r.th_lo[i] = (float)(tp - (double)r.th_hi[i]);
+  }
   return r;
 }
 
@@ -157,6 +162,7 @@ constexpr size_t kAlign = 256;
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Plan {
+  bool tc_attn = false;
   int n_split = 1, split_len = 0;
   size_t off_scores = 0, off_topk = 0, off_po = 0, off_pml = 0, off_tc = 0, total = 0;
 };
@@ -166,8 +172,14 @@ Plan make_plan(const csa_config* c, int B, int S, int64_t n_cap) {
   const bool hca = c->top_k == 0;
   const int64_t c_max = (int64_t)c->window + (hca ? n_cap : c->top_k);
   if (S == 1) {                               // decode: split the candidates across CTAs
-    p.split_len = use_tc_attn(c) ? tc_attn_split_len() : 64;
-    p.n_split = (int)((c_max + p.split_len - 1) / p.split_len);
+    p.tc_attn = use_tc_attn(c);
+    if (p.tc_attn) {
+      p.split_len = tc_attn_split_len();
+      p.n_split = tc_attn_splits(c->window, c->top_k, n_cap);
+    } else {
+      p.split_len = 64;
+      p.n_split = (int)((c_max + p.split_len - 1) / p.split_len);
+    }
     if (p.n_split < 1) p.n_split = 1;
   } else {
     p.split_len = (int)c_max;
@@ -179,7 +191,7 @@ Plan make_plan(const csa_config* c, int B, int S, int64_t n_cap) {
     p.off_scores = o; o = up(o + rows * (size_t)n_cap * sizeof(float));
     p.off_topk = o;   o = up(o + rows * (size_t)c->top_k * sizeof(int32_t));
   }
-  if (p.n_split > 1) {
+  if (p.n_split > 1 || p.tc_attn) {
     p.off_po = o;  o = up(o + rows * p.n_split * (size_t)c->H * c->d * sizeof(float));
     p.off_pml = o; o = up(o + rows * p.n_split * (size_t)c->H * 2 * sizeof(float));
   }
@@ -251,13 +263,13 @@ csa_status run_attn(const csa_config* c, const Plan& pl, int B, int S, const int
   ap.out = out; ap.pos = pos; ap.N = N; ap.n_cap = n_cap; ap.S = S; ap.H = c->H; ap.k = c->top_k;
   ap.ratio = c->ratio; ap.window = c->window; ap.n_split = pl.n_split; ap.split_len = pl.split_len;
   ap.scale = softmax_scale(c); ap.rope = make_rope(c); ap.err = device_error_word();
-  if (pl.n_split > 1) { ap.part_o = carve<float>(ws, pl.off_po); ap.part_ml = carve<float>(ws, pl.off_pml); }
+  if (pl.n_split > 1 || pl.tc_attn) { ap.part_o = carve<float>(ws, pl.off_po); ap.part_ml = carve<float>(ws, pl.off_pml); }
   const bool bf16 = c->storage == CSA_BF16;
   cudaError_t e;
-  if (use_tc_attn(c)) e = launch_stage(ST_ATTN, st, [&] { return tc_sparse_attn(B, ap, carve<char>(ws, pl.off_tc), st); });
+  if (pl.tc_attn) e = launch_stage(ST_ATTN, st, [&] { return tc_sparse_attn(B, ap, carve<char>(ws, pl.off_tc), st); });
   else e = launch_stage(ST_ATTN, st, [&] { return launch_attn_simt(bf16, B, ap, st); });
   if (e != cudaSuccess) return cuda_status(e, "attention launch");
-  if (pl.n_split <= 1) return CSA_OK;
+  if (pl.n_split <= 1 && !pl.tc_attn) return CSA_OK;
   return cuda_status(launch_stage(ST_MERGE, st, [&] { return launch_attn_merge(bf16, B, ap, st); }), "merge launch");
 }
 

@@ -54,8 +54,8 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnParams p)
   __shared__ __align__(16) float qs[kHG * kD];        // rotated query of this head group
   __shared__ __align__(16) float rows[kChunk * kD];   // staged candidate rows
   __shared__ int valid[kChunk];
-  __shared__ double theta[32];
-  if (threadIdx.x < 32) theta[threadIdx.x] = p.rope.theta[threadIdx.x];
+  __shared__ float th_hi[32], th_lo[32];
+  if (threadIdx.x < 32) { th_hi[threadIdx.x] = p.rope.th_hi[threadIdx.x]; th_lo[threadIdx.x] = p.rope.th_lo[threadIdx.x]; }
   __syncthreads();
 
   const int b = blockIdx.z, s = blockIdx.y;
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnParams p)
     if (h0 + h < p.H) { a = to_f32(q[(h0 + h) * kD + 2 * pr]); c2 = to_f32(q[(h0 + h) * kD + 2 * pr + 1]); }
     if (2 * pr >= r0) {
       float c, sn;
-      rope_cs(t, theta[(2 * pr - r0) / 2], c, sn);
+      rope_cs(t, th_hi[(2 * pr - r0) / 2], th_lo[(2 * pr - r0) / 2], c, sn);
       const float x = a * c - c2 * sn, y = a * sn + c2 * c;
       a = x; c2 = y;
     }
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnParams p)
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             float c, sn;
-            rope_cs(cd.rope_pos, theta[(d0 - r0) / 2 + k], c, sn);
+            rope_cs(cd.rope_pos, th_hi[(d0 - r0) / 2 + k], th_lo[(d0 - r0) / 2 + k], c, sn);
             const float x = v[2 * k], y = v[2 * k + 1];
             v[2 * k] = x * c - y * sn;
             v[2 * k + 1] = x * sn + y * c;
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnParams p)
       if (dim >= r0) {                        // inverse RoPE: pair partner is the neighbouring lane
         const float y = __shfl_xor_sync(0xffffffffu, x, 1);
         float c, sn;
-        rope_cs(t, theta[(dim - r0) / 2], c, sn);
+        rope_cs(t, th_hi[(dim - r0) / 2], th_lo[(dim - r0) / 2], c, sn);
         x = (lane & 1) ? (y * -sn + x * c) : (x * c + y * sn);
       }
       from_f32(op[dim], x);
@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnParams p) {
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       float c, sn;
-      rope_cs(t, p.rope.theta[(d0 - r0) / 2 + q], c, sn);
+      rope_cs(t, p.rope, (d0 - r0) / 2 + q, c, sn);
       const float x = acc[2 * q], y = acc[2 * q + 1];
       acc[2 * q] = x * c + y * sn;
       acc[2 * q + 1] = -x * sn + y * c;

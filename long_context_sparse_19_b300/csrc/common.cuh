@@ -60,20 +60,31 @@ __device__ __forceinline__ void from_f32(float& d, float x) { d = x; }
 __device__ __forceinline__ void from_f32(__nv_bfloat16& d, float x) { d = __float2bfloat16_rn(x); }
 
 // ------------------------------------------------------------------ RoPE
-// Rotary table: theta[i] = base^(-2i/d_rope) in double, computed on the host.
+// Rotary table. theta_i = base^(-2i/d_rope); the kernels use theta_i / pi split into two floats
+// (hi + lo, about 48 significant bits), computed in double on the host.
 struct RopeTab {
-  double theta[32];
+  float th_hi[32];
+  float th_lo[32];
   int d_rope;      // <= 64
 };
 
-// cos / sin of pos * theta. The angle is formed and reduced in double (in units of pi, to
-// [-1, 1]) so that positions up to 2^24 keep a float-accurate angle; sincospif of the reduced value
-// then needs no large-argument reduction.
-__device__ __forceinline__ void rope_cs(int64_t pos, double theta, float& c, float& s) {
-  const double kInvPi = 0.31830988618379067153776752674503;
-  double u = (double)pos * theta * kInvPi;
-  u -= 2.0 * rint(0.5 * u);
-  sincospif((float)u, &s, &c);
+// cos / sin of pos * theta_i without double arithmetic. u = pos * theta_i / pi is formed as an
+// unevaluated float sum: TwoProduct with FMA (Ogita, Rump and Oishi, "Accurate sum and dot
+// product", 2005) gives pos * th_hi exactly as p + e, and pos * th_lo is added to the error term.
+// Subtracting the even integer nearest to p is exact, which reduces u to [-1, 1] half-turns
+// (Cody and Waite style reduction with an exactly representable period); sincospif then needs no
+// argument reduction of its own. Positions must be < 2^24 (exact in float).
+__device__ __forceinline__ void rope_cs(int64_t pos, float th_hi, float th_lo, float& c, float& s) {
+  const float x = (float)pos;
+  const float p = x * th_hi;
+  const float e = fmaf(x, th_hi, -p);
+  const float lo = fmaf(x, th_lo, e);
+  const float r = (p - 2.0f * rintf(0.5f * p)) + lo;
+  sincospif(r, &s, &c);
+}
+
+__device__ __forceinline__ void rope_cs(int64_t pos, const RopeTab& tab, int i, float& c, float& s) {
+  rope_cs(pos, tab.th_hi[i], tab.th_lo[i], c, s);
 }
 
 // ------------------------------------------------------------------ reductions

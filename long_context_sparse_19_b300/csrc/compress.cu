@@ -115,7 +115,7 @@ __device__ void compress_run(const CompressParams& p, const CompressJob& job, in
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         float c, s;
-        rope_cs(e * m, p.rope.theta[(c0 - r0) / 2 + q], c, s);
+        rope_cs(e * m, p.rope, (c0 - r0) / 2 + q, c, s);
         const float a = x[2 * q], bq = x[2 * q + 1];
         x[2 * q] = a * c - bq * s;
         x[2 * q + 1] = a * s + bq * c;
@@ -132,21 +132,10 @@ __device__ void compress_block(const CompressParams& p, const CompressJob& job, 
   const int team = threadIdx.x / TPE;
   const int tt = threadIdx.x % TPE;
   const int b = blockIdx.y;
-  int64_t e_begin, e_end;
-  if (p.pos) {                                        // close mode: one entry per request
-    if (blockIdx.x != 0 || team != 0) return;
-    const int64_t t = p.pos[b];
-    if (t < 0 || t >= p.N) { if (tt == 0) set_error(p.err, DEVERR_BAD_POS); return; }
-    if ((t + 1) % p.ratio != 0) return;
-    e_begin = t / p.ratio;
-    if (e_begin >= p.n_cap) { if (tt == 0) set_error(p.err, DEVERR_BAD_POS); return; }
-    e_end = e_begin + 1;
-  } else {
-    constexpr int EPT = kEntriesPerBlock / TEAMS;
-    e_begin = p.first_entry + (int64_t)blockIdx.x * kEntriesPerBlock + (int64_t)team * EPT;
-    e_end = min(e_begin + EPT, p.first_entry + p.n_entries);
-    if (e_begin >= e_end) return;
-  }
+  constexpr int EPT = kEntriesPerBlock / TEAMS;
+  const int64_t e_begin = p.first_entry + (int64_t)blockIdx.x * kEntriesPerBlock + (int64_t)team * EPT;
+  const int64_t e_end = min(e_begin + EPT, p.first_entry + p.n_entries);
+  if (e_begin >= e_end) return;
   compress_run<T, C>(p, job, b, e_begin, e_end, team, tt, red);
 }
 
@@ -158,11 +147,140 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressParams
   else compress_block<T, 128>(p, job, red);
 }
 
+// ------------------------------------------------------------------ decode: the closing entry only
+// One CTA per (request, cache): when t closes a group, entry e = t/m is pooled from its 2m tokens.
+// The tokens are spread over G groups of threads (each thread: 8 channels of every G-th token,
+// one online-softmax state), so the loads of all tokens are in flight at once; the G partial
+// states per channel are then merged in shared memory, one thread per channel.
+constexpr int kCloseThreads = 512;
+
+template <typename T, int C>
+__device__ void compress_close(const CompressParams& p, const CompressJob& job, float* sm) {
+  constexpr int CH = C / 8;                  // channel chunks
+  constexpr int G = kCloseThreads / CH;      // token groups
+  const int b = blockIdx.x;
+  const int64_t t = p.pos[b];
+  if (t < 0 || t >= p.N) { if (threadIdx.x == 0) set_error(p.err, DEVERR_BAD_POS); return; }
+  if ((t + 1) % p.ratio != 0) return;
+  const int64_t e = t / p.ratio;
+  if (e >= p.n_cap) { if (threadIdx.x == 0) set_error(p.err, DEVERR_BAD_POS); return; }
+  const int m = p.ratio;
+  const int chunk = threadIdx.x % CH, g = threadIdx.x / CH;
+  const int c0 = chunk * 8;
+  const T* src = reinterpret_cast<const T*>(job.src) + (int64_t)b * p.N * C;
+  const T* gate = reinterpret_cast<const T*>(job.gate) + (int64_t)b * p.N * C;
+  Stat8 st;
+  st.clear();
+  const int64_t j0 = (e - 1) * m;                  // window position q holds token j0 + q
+  for (int pp = g; pp < 2 * m; pp += 4 * G) {
+    float v[4][8], gt[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {                  // issue up to four tokens' loads first
+      const int q = pp + u * G;
+      if (q < 2 * m && j0 + q >= 0) {
+        load8(src + (j0 + q) * C + c0, v[u]);
+        load8(gate + (j0 + q) * C + c0, gt[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = pp + u * G;
+      if (q < 2 * m && j0 + q >= 0) {
+        float bq[8];
+        load8(job.bias + (int64_t)q * C + c0, bq);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) st.add(k, gt[u][k] + bq[k], v[u][k]);
+      }
+    }
+  }
+  // partial states -> shared memory [3][G][C]
+  float* smx = sm;
+  float* ssum = sm + G * C;
+  float* sacc = sm + 2 * G * C;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    smx[g * C + c0 + k] = st.mx[k];
+    ssum[g * C + c0 + k] = st.sum[k];
+    sacc[g * C + c0 + k] = st.acc[k];
+  }
+  __syncthreads();
+  float* xs = sm + 3 * G * C;                      // [C] pooled values
+  float* red = xs + C;                             // [32]
+  float ss = 0.f;
+  if (threadIdx.x < C) {
+    const int c = threadIdx.x;
+    float M = -INFINITY;
+    for (int q = 0; q < G; ++q) M = fmaxf(M, smx[q * C + c]);
+    float num = 0.f, den = 0.f;
+    for (int q = 0; q < G; ++q) {
+      const float mq = smx[q * C + c];
+      if (mq == -INFINITY) continue;
+      const float a = expf(mq - M);
+      num = fmaf(sacc[q * C + c], a, num);
+      den = fmaf(ssum[q * C + c], a, den);
+    }
+    const float x = num / den;
+    xs[c] = x;
+    ss = x * x;
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < CH) {
+    float tot = 0.f;
+    for (int w = 0; w < kCloseThreads / 32; ++w) tot += red[w];
+    const float inv = 1.0f / sqrtf(tot / (float)C + p.eps);
+    float x[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = xs[c0 + k] * inv;
+    const int r0 = C - p.rope.d_rope;
+    if (c0 >= r0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float cs, sn;
+        rope_cs(e * m, p.rope, (c0 - r0) / 2 + q, cs, sn);
+        const float a = x[2 * q], bq = x[2 * q + 1];
+        x[2 * q] = a * cs - bq * sn;
+        x[2 * q + 1] = a * sn + bq * cs;
+      }
+    }
+    T* dst = reinterpret_cast<T*>(job.dst) + ((int64_t)b * p.n_cap + e) * C;
+    store8(dst + c0, x);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kCloseThreads) compress_close_kernel(const CompressParams p) {
+  extern __shared__ float sm[];
+  const CompressJob& job = p.job[blockIdx.y];
+  if (job.C == 512) compress_close<T, 512>(p, job, sm);
+  else compress_close<T, 128>(p, job, sm);
+}
+
 }  // namespace
 
 cudaError_t launch_compress(bool bf16, int B, const CompressParams& p, cudaStream_t st) {
-  const int64_t nb = p.pos ? 1 : (p.n_entries + kEntriesPerBlock - 1) / kEntriesPerBlock;
-  if (nb == 0 || B == 0) return cudaSuccess;
+  if (B == 0) return cudaSuccess;
+  if (p.pos) {
+    // shared memory: 3 partial states x (token groups x channels), which is kCloseThreads * 8 for
+    // both caches, plus the pooled row and reduction scratch
+    const size_t smem = (size_t)(3 * kCloseThreads * 8 + 512 + 32) * sizeof(float);
+    dim3 grid((unsigned)B, (unsigned)p.n_jobs);
+    cudaError_t e;
+    if (bf16) {
+      e = cudaFuncSetAttribute(compress_close_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+      if (e != cudaSuccess) return e;
+      compress_close_kernel<__nv_bfloat16><<<grid, kCloseThreads, smem, st>>>(p);
+    } else {
+      e = cudaFuncSetAttribute(compress_close_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      compress_close_kernel<float><<<grid, kCloseThreads, smem, st>>>(p);
+    }
+    return cudaGetLastError();
+  }
+  const int64_t nb = (p.n_entries + kEntriesPerBlock - 1) / kEntriesPerBlock;
+  if (nb == 0) return cudaSuccess;
   dim3 grid((unsigned)nb, (unsigned)B, (unsigned)p.n_jobs);
   if (bf16) compress_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(p);
   else compress_kernel<float><<<grid, kThreads, 0, st>>>(p);

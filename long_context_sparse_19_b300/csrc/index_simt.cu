@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(kTile) index_simt_kernel(const IndexParams p) 
       const int r0 = kDI - p.rope.d_rope;
       if (2 * pr >= r0) {
         float c, sn;
-        rope_cs(t, p.rope.theta[(2 * pr - r0) / 2], c, sn);
+        rope_cs(t, p.rope, (2 * pr - r0) / 2, c, sn);
         const float x = a * c - c2 * sn, y = a * sn + c2 * c;
         a = x; c2 = y;
       }

@@ -11,11 +11,12 @@ namespace csa {
 bool tc_index_available();                                    // the tcgen05 indexer is built
 bool tc_attn_available();                                     // the tcgen05 attention is built
 int tc_attn_split_len();                                      // candidates per attention CTA (decode)
+int tc_attn_splits(int window, int top_k, int64_t n_cap);     // CTAs per query: window + compressed tiles
 size_t tc_workspace_bytes(int B, int S, int64_t n_cap, int top_k);
 int tc_sm_count();
 
-// 2-D bf16 tensor map over [rows][128] with a 64-element x box_rows box and the 128-byte swizzle.
-cudaError_t make_tmap_rows128(CUtensorMap* map, const void* base, int64_t rows, uint32_t box_rows);
+// 2-D bf16 tensor map over [rows][cols] with a 64-element x box_rows box and the 128-byte swizzle.
+cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, int64_t rows, uint32_t cols, uint32_t box_rows);
 
 // s_i = sum_h w_h relu(rope(q_h, t) . cidx_i) for i < visible(t), bf16 operands, fp32 accumulate.
 cudaError_t tc_index_scores(int B, int S, const int64_t* pos, const void* q_idx, const float* w,

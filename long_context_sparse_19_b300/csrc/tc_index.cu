@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           float cs, sn;
-          rope_cs(t, p.rope.theta[(c * 8 - r0) / 2 + k], cs, sn);
+          rope_cs(t, p.rope, (c * 8 - r0) / 2 + k, cs, sn);
           const float a = x[2 * k], bb = x[2 * k + 1];
           x[2 * k] = a * cs - bb * sn;
           x[2 * k + 1] = a * sn + bb * cs;
@@ -203,12 +203,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-// 2-D bf16 tensor map [rows][128] with a 64 x box_rows box and the 128-byte swizzle.
-cudaError_t make_tmap_rows128(CUtensorMap* map, const void* base, int64_t rows, uint32_t box_rows) {
+// 2-D bf16 tensor map [rows][cols] with a 64 x box_rows box and the 128-byte swizzle.
+cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, int64_t rows, uint32_t cols, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {128 * 2};
+  const cuuint64_t dims[2] = {cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
   const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -216,6 +216,8 @@ cudaError_t make_tmap_rows128(CUtensorMap* map, const void* base, int64_t rows, 
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
+
+bool tc_index_available() { return true; }
 
 int tc_sm_count() {
   static int n = 0;
@@ -238,7 +240,7 @@ cudaError_t tc_index_scores(int B, int S, const int64_t* pos, const void* q_idx,
     attr = true;
   }
   CUtensorMap map;
-  cudaError_t e = make_tmap_rows128(&map, cidx, (int64_t)B * n_cap, kTileM);
+  cudaError_t e = make_tmap_2d(&map, cidx, (int64_t)B * n_cap, kDI, kTileM);
   if (e != cudaSuccess) return e;
   IndexTcParams p;
   p.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
