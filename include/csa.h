@@ -122,9 +122,10 @@ csa_status csa_compress(const csa_config* cfg, int32_t B, const csa_cache* cache
  *   q_idx   [B, S, H_idx, d_idx] storage (before RoPE; rotated at t inside)
  *   w       [B, S, H_idx] float32 signed head weights
  *   cidx    [B, n_cap, d_idx] storage
- *   topk    [B, S, top_k] int32 out: the top_k visible entries by
- *           s_i = sum_h w_h * max(0, rope(q_h, t) . cidx_i), ordered by (-s_i, i); when fewer than
- *           top_k entries are visible, the tail holds -1.
+ *   topk    [B, S, top_k] int32 out: the top_k visible entries under the order (-s_i, i) with
+ *           s_i = sum_h w_h * max(0, rope(q_h, t) . cidx_i) (of equal scores the lower index wins),
+ *           written in ascending entry index; when fewer than top_k entries are visible, every
+ *           visible entry is taken and the tail holds -1.
  *   scores  [B, S, n_cap] float32 out, nullable: s_i for i < visible(t); other entries untouched.
  * Requires top_k > 0. */
 csa_status csa_index_topk(const csa_config* cfg, int32_t B, int32_t S, const int64_t* pos,

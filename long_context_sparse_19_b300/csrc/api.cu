@@ -163,8 +163,9 @@ size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Plan {
   bool tc_attn = false;
+  bool tc_prefill = false;           // one CTA per query over all candidates, no partials
   int n_split = 1, split_len = 0;
-  size_t off_scores = 0, off_topk = 0, off_po = 0, off_pml = 0, off_tc = 0, total = 0;
+  size_t off_scores = 0, off_topk = 0, off_tksel = 0, off_po = 0, off_pml = 0, off_tc = 0, total = 0;
 };
 
 Plan make_plan(const csa_config* c, int B, int S, int64_t n_cap) {
@@ -175,7 +176,7 @@ Plan make_plan(const csa_config* c, int B, int S, int64_t n_cap) {
     p.tc_attn = use_tc_attn(c);
     if (p.tc_attn) {
       p.split_len = tc_attn_split_len();
-      p.n_split = tc_attn_splits(c->window, c->top_k, n_cap);
+      p.n_split = tc_attn_splits(c->window, c->top_k, n_cap, B * S);
     } else {
       p.split_len = 64;
       p.n_split = (int)((c_max + p.split_len - 1) / p.split_len);
@@ -184,12 +185,15 @@ Plan make_plan(const csa_config* c, int B, int S, int64_t n_cap) {
   } else {
     p.split_len = (int)c_max;
     p.n_split = 1;
+    const int64_t tiles = (c->window + 127) / 128 + (hca ? (n_cap + 127) / 128 : (c->top_k + 127) / 128);
+    p.tc_prefill = use_tc_attn(c) && tiles <= tc_attn_prefill_max_tiles();
   }
   size_t o = 0;
   const size_t rows = (size_t)B * (size_t)S;
   if (!hca) {
     p.off_scores = o; o = up(o + rows * (size_t)n_cap * sizeof(float));
     p.off_topk = o;   o = up(o + rows * (size_t)c->top_k * sizeof(int32_t));
+    p.off_tksel = o;  o = up(o + topk_workspace_bytes((int64_t)rows, n_cap, c->top_k));
   }
   if (p.n_split > 1 || p.tc_attn) {
     p.off_po = o;  o = up(o + rows * p.n_split * (size_t)c->H * c->d * sizeof(float));
@@ -224,19 +228,21 @@ csa_status run_compress(const csa_config* c, int B, const csa_cache* k, int64_t 
   }
   p.N = k->N; p.n_cap = k->n_cap; p.first_entry = first; p.n_entries = n; p.pos = pos;
   p.ratio = c->ratio; p.eps = c->rms_eps; p.rope = make_rope(c); p.err = device_error_word();
-  return cuda_status(launch_stage(ST_COMPRESS, st, [&] { return launch_compress(c->storage == CSA_BF16, B, p, st); }),
-                     "compress launch");
+  // the compressor is the first kernel of every call that runs it: a normal (fully ordered) launch
+  return cuda_status(
+      launch_stage(ST_COMPRESS, st, [&] { return launch_compress(c->storage == CSA_BF16, B, p, st, false); }),
+      "compress launch");
 }
 
 csa_status run_index_topk(const csa_config* c, int B, int S, const int64_t* pos, const void* q_idx,
                           const float* w, const void* cidx, int64_t n_cap, int32_t* topk,
-                          float* scores, void* tc_ws, cudaStream_t st) {
+                          float* scores, void* tk_ws, void* tc_ws, cudaStream_t st, bool pdl) {
   const bool bf16 = c->storage == CSA_BF16;
   if (use_tc_index(c)) {
     const RopeTab rope = make_rope(c);
     int32_t* err = device_error_word();
     cudaError_t e = launch_stage(ST_INDEX, st, [&] {
-      return tc_index_scores(B, S, pos, q_idx, w, cidx, n_cap, c->ratio, rope, scores, tc_ws, err, st);
+      return tc_index_scores(B, S, pos, q_idx, w, cidx, n_cap, c->ratio, rope, scores, tc_ws, err, st, pdl);
     });
     if (e != cudaSuccess) return cuda_status(e, "tcgen05 indexer launch");
   } else {
@@ -244,19 +250,19 @@ csa_status run_index_topk(const csa_config* c, int B, int S, const int64_t* pos,
     memset(&ip, 0, sizeof ip);
     ip.q_idx = q_idx; ip.w = w; ip.cidx = cidx; ip.scores = scores; ip.pos = pos; ip.n_cap = n_cap;
     ip.S = S; ip.H_idx = c->H_idx; ip.ratio = c->ratio; ip.rope = make_rope(c);
-    csa_status s = cuda_status(launch_stage(ST_INDEX, st, [&] { return launch_index_simt(bf16, B, ip, st); }),
+    csa_status s = cuda_status(launch_stage(ST_INDEX, st, [&] { return launch_index_simt(bf16, B, ip, st, pdl); }),
                                "indexer launch");
     if (s != CSA_OK) return s;
   }
   TopkParams tp;
   tp.scores = scores; tp.topk = topk; tp.pos = pos; tp.n_cap = n_cap; tp.S = S; tp.k = c->top_k;
-  tp.ratio = c->ratio;
-  return cuda_status(launch_stage(ST_TOPK, st, [&] { return launch_topk(B, tp, st); }), "top-k launch");
+  tp.ratio = c->ratio; tp.ws = tk_ws;
+  return cuda_status(launch_stage(ST_TOPK, st, [&] { return launch_topk(B, tp, st, true); }), "top-k launch");
 }
 
 csa_status run_attn(const csa_config* c, const Plan& pl, int B, int S, const int64_t* pos,
                     const void* q, const void* kv, int64_t N, const void* ckv, int64_t n_cap,
-                    const int32_t* topk, const float* sink, void* out, void* ws, cudaStream_t st) {
+                    const int32_t* topk, const float* sink, void* out, void* ws, cudaStream_t st, bool pdl) {
   AttnParams ap;
   memset(&ap, 0, sizeof ap);
   ap.q = q; ap.kv = kv; ap.ckv = ckv; ap.topk = c->top_k > 0 ? topk : nullptr; ap.sink = sink;
@@ -266,11 +272,16 @@ csa_status run_attn(const csa_config* c, const Plan& pl, int B, int S, const int
   if (pl.n_split > 1 || pl.tc_attn) { ap.part_o = carve<float>(ws, pl.off_po); ap.part_ml = carve<float>(ws, pl.off_pml); }
   const bool bf16 = c->storage == CSA_BF16;
   cudaError_t e;
-  if (pl.tc_attn) e = launch_stage(ST_ATTN, st, [&] { return tc_sparse_attn(B, ap, carve<char>(ws, pl.off_tc), st); });
-  else e = launch_stage(ST_ATTN, st, [&] { return launch_attn_simt(bf16, B, ap, st); });
+  if (pl.tc_prefill) {
+    e = launch_stage(ST_ATTN, st, [&] { return tc_attn_prefill(B, ap, st, pdl); });
+    return cuda_status(e, "prefill attention launch");
+  }
+  if (pl.tc_attn) e = launch_stage(ST_ATTN, st, [&] { return tc_sparse_attn(B, ap, carve<char>(ws, pl.off_tc), st, pdl); });
+  else e = launch_stage(ST_ATTN, st, [&] { return launch_attn_simt(bf16, B, ap, st, pdl); });
   if (e != cudaSuccess) return cuda_status(e, "attention launch");
   if (pl.n_split <= 1 && !pl.tc_attn) return CSA_OK;
-  return cuda_status(launch_stage(ST_MERGE, st, [&] { return launch_attn_merge(bf16, B, ap, st); }), "merge launch");
+  return cuda_status(launch_stage(ST_MERGE, st, [&] { return launch_attn_merge(bf16, B, ap, st, true); }),
+                     "merge launch");
 }
 
 csa_status check_cache_ptrs(const csa_config* c, const csa_cache* k, bool need_idx) {
@@ -357,7 +368,8 @@ csa_status csa_index_topk(const csa_config* cfg, int32_t B, int32_t S, const int
   if (s != CSA_OK) return s;
   if (B == 0 || S == 0) return CSA_OK;
   float* sc = scores ? scores : carve<float>(ws, pl.off_scores);
-  return run_index_topk(cfg, B, S, pos, q_idx, w, cidx, n_cap, topk, sc, carve<char>(ws, pl.off_tc), stream);
+  return run_index_topk(cfg, B, S, pos, q_idx, w, cidx, n_cap, topk, sc, carve<char>(ws, pl.off_tksel),
+                        carve<char>(ws, pl.off_tc), stream, false);
 }
 
 csa_status csa_sparse_attn(const csa_config* cfg, int32_t B, int32_t S, const int64_t* pos, const void* q,
@@ -373,7 +385,7 @@ csa_status csa_sparse_attn(const csa_config* cfg, int32_t B, int32_t S, const in
   s = check_ws(pl, ws, ws_bytes);
   if (s != CSA_OK) return s;
   if (B == 0 || S == 0) return CSA_OK;
-  return run_attn(cfg, pl, B, S, pos, q, kv, N, ckv, n_cap, topk, sink, out, ws, stream);
+  return run_attn(cfg, pl, B, S, pos, q, kv, N, ckv, n_cap, topk, sink, out, ws, stream, false);
 }
 
 csa_status csa_decode(const csa_config* cfg, int32_t B, const int64_t* pos, const csa_cache* cache,
@@ -397,11 +409,12 @@ csa_status csa_decode(const csa_config* cfg, int32_t B, const int64_t* pos, cons
   if (!hca) {
     tk = topk_out ? topk_out : carve<int32_t>(ws, pl.off_topk);
     s = run_index_topk(cfg, B, 1, pos, q_idx, w, cache->cidx, cache->n_cap, tk,
-                       carve<float>(ws, pl.off_scores), carve<char>(ws, pl.off_tc), stream);
+                       carve<float>(ws, pl.off_scores), carve<char>(ws, pl.off_tksel), carve<char>(ws, pl.off_tc),
+                       stream, true);
     if (s != CSA_OK) return s;
   }
   return run_attn(cfg, pl, B, 1, pos, q, cache->kv, cache->N, cache->ckv, cache->n_cap, tk, sink, out, ws,
-                  stream);
+                  stream, true);
 }
 
 csa_status csa_prefill(const csa_config* cfg, int32_t B, int32_t S, const csa_cache* cache, const void* q,
@@ -427,11 +440,12 @@ csa_status csa_prefill(const csa_config* cfg, int32_t B, int32_t S, const csa_ca
   if (!hca) {
     tk = topk_out ? topk_out : carve<int32_t>(ws, pl.off_topk);
     s = run_index_topk(cfg, B, S, nullptr, q_idx, w, cache->cidx, cache->n_cap, tk,
-                       carve<float>(ws, pl.off_scores), carve<char>(ws, pl.off_tc), stream);
+                       carve<float>(ws, pl.off_scores), carve<char>(ws, pl.off_tksel), carve<char>(ws, pl.off_tc),
+                       stream, true);
     if (s != CSA_OK) return s;
   }
   return run_attn(cfg, pl, B, S, nullptr, q, cache->kv, cache->N, cache->ckv, cache->n_cap, tk, sink, out,
-                  ws, stream);
+                  ws, stream, true);
 }
 
 int64_t csa_launch_count(void) { return g_launches.load(); }

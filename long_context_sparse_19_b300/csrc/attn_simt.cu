@@ -55,6 +55,8 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnParams p)
   __shared__ __align__(16) float rows[kChunk * kD];   // staged candidate rows
   __shared__ int valid[kChunk];
   __shared__ float th_hi[32], th_lo[32];
+  griddep_launch();
+  griddep_wait();
   if (threadIdx.x < 32) { th_hi[threadIdx.x] = p.rope.th_hi[threadIdx.x]; th_lo[threadIdx.x] = p.rope.th_lo[threadIdx.x]; }
   __syncthreads();
 
@@ -197,35 +199,66 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnParams p)
 }
 
 // Merge of split partials: M = max(m_i, sink), L = sum_i l_i e^(m_i - M) + e^(sink - M),
-// o = sum_i e^(m_i - M) o_i / L, then the inverse RoPE at t.
+// o = sum_i e^(m_i - M) o_i / L, then the inverse RoPE at t. One CTA per (query, 8 heads): warp w
+// owns head 8 blockIdx.x + w, lane l owns dims 16 l .. 16 l + 15 (four float4 per split); the
+// split weights are computed lane-parallel and broadcast with shuffles.
+constexpr int kMergeHeads = 8;
+
 template <typename T>
-__global__ void __launch_bounds__(128) attn_merge_kernel(const AttnParams p) {
-  const int h = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
+__global__ void __launch_bounds__(32 * kMergeHeads) attn_merge_kernel(const AttnParams p) {
+  griddep_launch();
+  griddep_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x * kMergeHeads + warp;
+  const int s = blockIdx.y, b = blockIdx.z;
+  if (h >= p.H) return;
   const int64_t row = (int64_t)b * p.S + s;
   const int64_t t = p.pos ? p.pos[row] : s;
   const float sk = p.sink[h];
+  const float* ml = p.part_ml + (row * p.n_split * p.H + h) * 2;     // split i at ml[2 * i * H]
+  const int64_t mstride = 2 * (int64_t)p.H;
   float M = sk;
-  for (int i = 0; i < p.n_split; ++i) M = fmaxf(M, p.part_ml[2 * ((row * p.n_split + i) * p.H + h)]);
-  float L = expf(sk - M);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  const int d0 = threadIdx.x * 4;
-  for (int i = 0; i < p.n_split; ++i) {
-    const int64_t pi = (row * p.n_split + i) * p.H + h;
-    const float mi = p.part_ml[2 * pi];
-    if (mi == -INFINITY) continue;
-    const float a = expf(mi - M);
-    L = fmaf(p.part_ml[2 * pi + 1], a, L);
-    const float4 v = *reinterpret_cast<const float4*>(p.part_o + pi * kD + d0);
-    acc[0] = fmaf(a, v.x, acc[0]); acc[1] = fmaf(a, v.y, acc[1]);
-    acc[2] = fmaf(a, v.z, acc[2]); acc[3] = fmaf(a, v.w, acc[3]);
+  for (int i = lane; i < p.n_split; i += 32) M = fmaxf(M, ml[i * mstride]);
+  M = warp_max(M);
+  float L = 0.f;
+  for (int i = lane; i < p.n_split; i += 32) {
+    const float mi = ml[i * mstride];
+    if (mi != -INFINITY) L = fmaf(ml[i * mstride + 1], expf(mi - M), L);
+  }
+  L = warp_sum(L) + expf(sk - M);
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  const int d0 = lane * 16;
+  const float* po = p.part_o + (row * p.n_split * p.H + h) * kD + d0;
+  const int64_t ostride = (int64_t)p.H * kD;
+  for (int i0 = 0; i0 < p.n_split; i0 += 32) {
+    const int i = i0 + lane;
+    const float mi = i < p.n_split ? ml[i * mstride] : -INFINITY;
+    const float wgt = mi == -INFINITY ? 0.f : expf(mi - M);
+    const int cnt = min(32, p.n_split - i0);
+#pragma unroll 2
+    for (int u = 0; u < cnt; ++u) {
+      const float a = __shfl_sync(0xffffffffu, wgt, u);
+      if (a == 0.f) continue;
+      const float4* src = reinterpret_cast<const float4*>(po + (int64_t)(i0 + u) * ostride);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = src[q];
+        acc[4 * q + 0] = fmaf(a, v.x, acc[4 * q + 0]);
+        acc[4 * q + 1] = fmaf(a, v.y, acc[4 * q + 1]);
+        acc[4 * q + 2] = fmaf(a, v.z, acc[4 * q + 2]);
+        acc[4 * q + 3] = fmaf(a, v.w, acc[4 * q + 3]);
+      }
+    }
   }
   const float inv = 1.f / L;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) acc[k] *= inv;
+  for (int k = 0; k < 16; ++k) acc[k] *= inv;
   const int r0 = kD - p.rope.d_rope;
   if (d0 >= r0) {
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < 8; ++q) {
       float c, sn;
       rope_cs(t, p.rope, (d0 - r0) / 2 + q, c, sn);
       const float x = acc[2 * q], y = acc[2 * q + 1];
@@ -234,27 +267,28 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnParams p) {
     }
   }
   T* op = reinterpret_cast<T*>(p.out) + (row * p.H + h) * kD + d0;
+  float a8[8], b8[8];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) from_f32(op[k], acc[k]);
+  for (int k = 0; k < 8; ++k) { a8[k] = acc[k]; b8[k] = acc[8 + k]; }
+  store8(op, a8);
+  store8(op + 8, b8);
 }
 
 }  // namespace
 
-cudaError_t launch_attn_simt(bool bf16, int B, const AttnParams& p, cudaStream_t st) {
+cudaError_t launch_attn_simt(bool bf16, int B, const AttnParams& p, cudaStream_t st, bool pdl) {
   if (B == 0 || p.S == 0) return cudaSuccess;
   const int n_hg = (p.H + kHG - 1) / kHG;
   dim3 grid((unsigned)(p.n_split * n_hg), (unsigned)p.S, (unsigned)B);
-  if (bf16) attn_simt_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(p);
-  else attn_simt_kernel<float><<<grid, kThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  if (bf16) return launch_kernel(pdl, attn_simt_kernel<__nv_bfloat16>, grid, dim3(kThreads), 0, st, p);
+  return launch_kernel(pdl, attn_simt_kernel<float>, grid, dim3(kThreads), 0, st, p);
 }
 
-cudaError_t launch_attn_merge(bool bf16, int B, const AttnParams& p, cudaStream_t st) {
+cudaError_t launch_attn_merge(bool bf16, int B, const AttnParams& p, cudaStream_t st, bool pdl) {
   if (B == 0 || p.S == 0 || p.n_split <= 1) return cudaSuccess;
-  dim3 grid((unsigned)p.H, (unsigned)p.S, (unsigned)B);
-  if (bf16) attn_merge_kernel<__nv_bfloat16><<<grid, 128, 0, st>>>(p);
-  else attn_merge_kernel<float><<<grid, 128, 0, st>>>(p);
-  return cudaGetLastError();
+  dim3 grid((unsigned)((p.H + kMergeHeads - 1) / kMergeHeads), (unsigned)p.S, (unsigned)B);
+  if (bf16) return launch_kernel(pdl, attn_merge_kernel<__nv_bfloat16>, grid, dim3(32 * kMergeHeads), 0, st, p);
+  return launch_kernel(pdl, attn_merge_kernel<float>, grid, dim3(32 * kMergeHeads), 0, st, p);
 }
 
 }  // namespace csa

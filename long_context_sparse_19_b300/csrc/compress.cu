@@ -142,6 +142,8 @@ __device__ void compress_block(const CompressParams& p, const CompressJob& job, 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressParams p) {
   __shared__ float red[16];
+  griddep_launch();
+  griddep_wait();
   const CompressJob& job = p.job[blockIdx.z];
   if (job.C == 512) compress_block<T, 512>(p, job, red);
   else compress_block<T, 128>(p, job, red);
@@ -252,6 +254,8 @@ __device__ void compress_close(const CompressParams& p, const CompressJob& job, 
 template <typename T>
 __global__ void __launch_bounds__(kCloseThreads) compress_close_kernel(const CompressParams p) {
   extern __shared__ float sm[];
+  griddep_launch();
+  griddep_wait();
   const CompressJob& job = p.job[blockIdx.y];
   if (job.C == 512) compress_close<T, 512>(p, job, sm);
   else compress_close<T, 128>(p, job, sm);
@@ -259,7 +263,7 @@ __global__ void __launch_bounds__(kCloseThreads) compress_close_kernel(const Com
 
 }  // namespace
 
-cudaError_t launch_compress(bool bf16, int B, const CompressParams& p, cudaStream_t st) {
+cudaError_t launch_compress(bool bf16, int B, const CompressParams& p, cudaStream_t st, bool pdl) {
   if (B == 0) return cudaSuccess;
   if (p.pos) {
     // shared memory: 3 partial states x (token groups x channels), which is kCloseThreads * 8 for
@@ -271,20 +275,19 @@ cudaError_t launch_compress(bool bf16, int B, const CompressParams& p, cudaStrea
       e = cudaFuncSetAttribute(compress_close_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
       if (e != cudaSuccess) return e;
-      compress_close_kernel<__nv_bfloat16><<<grid, kCloseThreads, smem, st>>>(p);
+      e = launch_kernel(pdl, compress_close_kernel<__nv_bfloat16>, grid, dim3(kCloseThreads), smem, st, p);
     } else {
       e = cudaFuncSetAttribute(compress_close_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
-      compress_close_kernel<float><<<grid, kCloseThreads, smem, st>>>(p);
+      e = launch_kernel(pdl, compress_close_kernel<float>, grid, dim3(kCloseThreads), smem, st, p);
     }
-    return cudaGetLastError();
+    return e;
   }
   const int64_t nb = (p.n_entries + kEntriesPerBlock - 1) / kEntriesPerBlock;
   if (nb == 0) return cudaSuccess;
   dim3 grid((unsigned)nb, (unsigned)B, (unsigned)p.n_jobs);
-  if (bf16) compress_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(p);
-  else compress_kernel<float><<<grid, kThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  if (bf16) return launch_kernel(pdl, compress_kernel<__nv_bfloat16>, grid, dim3(kThreads), 0, st, p);
+  return launch_kernel(pdl, compress_kernel<float>, grid, dim3(kThreads), 0, st, p);
 }
 
 }  // namespace csa

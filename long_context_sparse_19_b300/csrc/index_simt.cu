@@ -19,6 +19,8 @@ template <typename T>
 __global__ void __launch_bounds__(kTile) index_simt_kernel(const IndexParams p) {
   __shared__ float qs[kMaxHI][kDI];
   __shared__ float ws[kMaxHI];
+  griddep_launch();
+  griddep_wait();
   const int b = blockIdx.z, s = blockIdx.y;
   const int64_t t = p.pos ? p.pos[(int64_t)b * p.S + s] : s;
   const int64_t V = min(visible_entries(t, p.ratio), p.n_cap);
@@ -79,13 +81,12 @@ __global__ void __launch_bounds__(kTile) index_simt_kernel(const IndexParams p) 
 
 }  // namespace
 
-cudaError_t launch_index_simt(bool bf16, int B, const IndexParams& p, cudaStream_t st) {
+cudaError_t launch_index_simt(bool bf16, int B, const IndexParams& p, cudaStream_t st, bool pdl) {
   const int64_t nx = (p.n_cap + kTile - 1) / kTile;
   if (nx == 0 || B == 0 || p.S == 0) return cudaSuccess;
   dim3 grid((unsigned)nx, (unsigned)p.S, (unsigned)B);
-  if (bf16) index_simt_kernel<__nv_bfloat16><<<grid, kTile, 0, st>>>(p);
-  else index_simt_kernel<float><<<grid, kTile, 0, st>>>(p);
-  return cudaGetLastError();
+  if (bf16) return launch_kernel(pdl, index_simt_kernel<__nv_bfloat16>, grid, dim3(kTile), 0, st, p);
+  return launch_kernel(pdl, index_simt_kernel<float>, grid, dim3(kTile), 0, st, p);
 }
 
 }  // namespace csa

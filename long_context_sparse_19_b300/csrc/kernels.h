@@ -26,7 +26,8 @@ struct CompressParams {
   int32_t* err;
 };
 
-cudaError_t launch_compress(bool bf16, int B, const CompressParams& p, cudaStream_t st);
+// `pdl`: launch as a programmatic dependent of the previous kernel in the stream.
+cudaError_t launch_compress(bool bf16, int B, const CompressParams& p, cudaStream_t st, bool pdl);
 
 // ------------------------------------------------------------------ K2 / K6 indexer scores (SIMT)
 struct IndexParams {
@@ -40,7 +41,7 @@ struct IndexParams {
   RopeTab rope;
 };
 
-cudaError_t launch_index_simt(bool bf16, int B, const IndexParams& p, cudaStream_t st);
+cudaError_t launch_index_simt(bool bf16, int B, const IndexParams& p, cudaStream_t st, bool pdl);
 
 // ------------------------------------------------------------------ K3 top-k
 struct TopkParams {
@@ -49,9 +50,11 @@ struct TopkParams {
   const int64_t* pos;    // [B, S]; null: t = s
   int64_t n_cap;
   int S, k, ratio;
+  void* ws;              // candidate buffers of the multi-level selection (topk_workspace_bytes)
 };
 
-cudaError_t launch_topk(int B, const TopkParams& p, cudaStream_t st);
+size_t topk_workspace_bytes(int64_t rows, int64_t n_cap, int k);
+cudaError_t launch_topk(int B, const TopkParams& p, cudaStream_t st, bool pdl);
 
 // ------------------------------------------------------------------ K4 / K5 attention (SIMT)
 struct AttnParams {
@@ -71,7 +74,7 @@ struct AttnParams {
   int32_t* err;
 };
 
-cudaError_t launch_attn_simt(bool bf16, int B, const AttnParams& p, cudaStream_t st);
-cudaError_t launch_attn_merge(bool bf16, int B, const AttnParams& p, cudaStream_t st);
+cudaError_t launch_attn_simt(bool bf16, int B, const AttnParams& p, cudaStream_t st, bool pdl);
+cudaError_t launch_attn_merge(bool bf16, int B, const AttnParams& p, cudaStream_t st, bool pdl);
 
 }  // namespace csa

@@ -11,7 +11,7 @@ namespace csa {
 bool tc_index_available();                                    // the tcgen05 indexer is built
 bool tc_attn_available();                                     // the tcgen05 attention is built
 int tc_attn_split_len();                                      // candidates per attention CTA (decode)
-int tc_attn_splits(int window, int top_k, int64_t n_cap);     // CTAs per query: window + compressed tiles
+int tc_attn_splits(int window, int top_k, int64_t n_cap, int rows);   // CTAs per query (rows = B * S)
 size_t tc_workspace_bytes(int B, int S, int64_t n_cap, int top_k);
 int tc_sm_count();
 
@@ -21,9 +21,14 @@ cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, int64_t rows, uint3
 // s_i = sum_h w_h relu(rope(q_h, t) . cidx_i) for i < visible(t), bf16 operands, fp32 accumulate.
 cudaError_t tc_index_scores(int B, int S, const int64_t* pos, const void* q_idx, const float* w,
                             const void* cidx, int64_t n_cap, int ratio, const RopeTab& rope,
-                            float* scores, void* ws, int32_t* err, cudaStream_t st);
+                            float* scores, void* ws, int32_t* err, cudaStream_t st, bool pdl);
+
+// Many-query attention (prefill): one CTA per query over all of its candidates (at most
+// tc_attn_prefill_max_tiles() tiles of 128), final output written directly.
+int tc_attn_prefill_max_tiles();
+cudaError_t tc_attn_prefill(int B, const AttnParams& p, cudaStream_t st, bool pdl);
 
 // Sparse attention (split partials when p.n_split > 1, else the final output).
-cudaError_t tc_sparse_attn(int B, const AttnParams& p, void* ws, cudaStream_t st);
+cudaError_t tc_sparse_attn(int B, const AttnParams& p, void* ws, cudaStream_t st, bool pdl);
 
 }  // namespace csa

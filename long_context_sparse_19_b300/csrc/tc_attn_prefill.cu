@@ -1,0 +1,401 @@
+// K7: sparse joint attention for many queries (causal prefill) on the tensor cores (bf16, H = 64,
+// d = 512), one CTA per query owning its whole candidate set (at most 5 tiles of 128 candidates).
+//
+// [FLASH] "DeepSeek-V4-Flash 架构：一个 token 的旅程", sections "局部和压缩记忆，共用一次归一化" (one
+// softmax over the raw window and the selected compressed entries; the per-head sink enlarges the
+// denominator only) and "输出投影也分组，并且降低中间维度" (o = inverse_RoPE(o)).
+//
+// Because the CTA sees every candidate of its query, the softmax is exact in one pass and no split
+// partials exist:
+//   phase S: S^T[j] = KV_j Q^T for every tile j (M = 128 candidates, N = 64 heads, K = 512), all
+//            tiles kept in TMEM (5 x 64 columns);
+//   softmax: per-head max over every candidate and the sink, P^T = exp(scale s - max) in bf16 (it
+//            reuses the Q buffer, dead by then), per-head denominators;
+//   phase O: O^T[dims] = sum_j KV_j^T P^T_j in two halves of 256 dims (2 x 64 TMEM columns), each
+//            half normalised and written as the final output (inverse RoPE on dims 448..511).
+// The KV data streams through a 4-stage ring of 32 KB K-chunks twice (phase S, then phase O; the
+// second pass hits L2). Warps: 0 = Q TMA + tcgen05.mma issuer, 1 = TMEM owner + Q rotation,
+// 2..5 = softmax / epilogue (thread = TMEM lane), 6..7 = cp.async gather producers (raw window rows
+// are rotated at their own positions in shared memory).
+#include <cudaTypedefs.h>
+
+#include "tc.h"
+#include "tc_ptx.cuh"
+
+namespace csa {
+namespace {
+
+using namespace tc;
+
+constexpr int kD = 512;
+constexpr int kH = 64;
+constexpr int kTile = 128;
+constexpr int kMaxTiles = 5;
+constexpr int kThreads = 256;
+constexpr int kProducers = 64;                      // warps 6..7
+constexpr int kStages = 4;
+constexpr uint32_t kBlk = kTile * 128;              // 16 KB: [128 rows][64 dims] swizzled
+constexpr uint32_t kChunkBytes = 2 * kBlk;          // 32 KB: 128 rows x 128 dims
+constexpr uint32_t kQBlock = kH * 128;              // 8 KB: [64 heads][64 dims]
+constexpr uint32_t kQBytes = 8 * kQBlock;           // 64 KB
+constexpr uint32_t kPBytes = kTile * 128;           // 16 KB per tile
+constexpr uint32_t kQPBytes = kMaxTiles * kPBytes;  // 80 KB: Q (phase S), then P^T (phase O)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = kMaxTiles * kH;          // 320: O^T half, 2 x 64 columns
+constexpr uint32_t kIdescS = idesc_bf16(128, 64, false, false);
+constexpr uint32_t kIdescO = idesc_bf16(128, 64, true, true);
+constexpr size_t kAuxBytes = 5120;
+constexpr size_t kSmemBytes = 1024 + kQPBytes + kStages * kChunkBytes + kAuxBytes;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct PrefillParams {
+  const __nv_bfloat16* kv;   // [B, N, 512]
+  const __nv_bfloat16* ckv;  // [B, n_cap, 512]
+  const int32_t* topk;       // [B, S, k] or null (HCA)
+  const int64_t* pos;        // [B, S] or null (t = s)
+  const float* sink;         // [64]
+  __nv_bfloat16* out;        // [B, S, 64, 512]
+  int64_t N, n_cap;
+  int S, k, ratio, window, win_tiles, n_tiles;
+  float scale;
+  RopeTab rope;
+  int32_t* err;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* qs = smem;                                          // Q: [8 blocks][64 heads][128 B]
+  uint8_t* ps = smem;                                          // P^T: [5 tiles][128 rows][128 B] (after phase S)
+  uint8_t* ring = smem + kQPBytes;                             // kStages x [2 blocks][128 rows][128 B]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + kStages * kChunkBytes);
+  uint64_t* full = bars;                                       // [kStages] (kProducers arrivals)
+  uint64_t* empty = bars + kStages;                            // [kStages] (MMA commit)
+  uint64_t* bar_q = bars + 2 * kStages;                        // Q landed (tx)
+  uint64_t* bar_qrot = bar_q + 1;                              // Q rotated (32 arrivals)
+  uint64_t* bar_s = bar_q + 2;                                 // S^T complete
+  uint64_t* bar_p = bar_q + 3;                                 // P^T written (128 arrivals)
+  uint64_t* bar_o0 = bar_q + 4;                                // O^T half 0 complete
+  uint64_t* bar_e0 = bar_q + 5;                                // O^T half 0 read (128 arrivals)
+  uint64_t* bar_o1 = bar_q + 6;                                // O^T half 1 complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_q + 8);
+  int32_t* rows_s = reinterpret_cast<int32_t*>(bar_q + 10);    // [5][128] global row (-1 = empty)
+  float* th_hi = reinterpret_cast<float*>(rows_s + kMaxTiles * kTile);   // [32]
+  float* th_lo = th_hi + 32;                                   // [32]
+  float* red = th_lo + 32;                                     // [4][64]
+  float* mx_s = red + 4 * kH;                                  // [64] max of scale * s and the sink
+  float* il_s = mx_s + kH;                                     // [64] 1 / denominator
+
+  griddep_launch();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.y, s = blockIdx.x;
+  const int64_t row = (int64_t)b * p.S + s;
+  const int64_t t = p.pos ? p.pos[row] : s;
+  if (t < 0 || t >= p.N) {
+    if (threadIdx.x == 0) set_error(p.err, DEVERR_BAD_POS);
+    return;
+  }
+  const int64_t V = min(visible_entries(t, p.ratio), p.n_cap);
+  const int64_t lo = t - p.window + 1 > 0 ? t - p.window + 1 : 0;
+  const int64_t n_win = t - lo + 1;
+  const int nt = p.n_tiles;
+
+  if (threadIdx.x < 32) { th_hi[threadIdx.x] = p.rope.th_hi[threadIdx.x]; th_lo[threadIdx.x] = p.rope.th_lo[threadIdx.x]; }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], kProducers); mbar_init(&empty[i], 1); }
+    mbar_init(bar_q, 1);
+    mbar_init(bar_qrot, 32);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_p, 128);
+    mbar_init(bar_o0, 1);
+    mbar_init(bar_e0, 128);
+    mbar_init(bar_o1, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&qmap);
+    mbar_arrive_expect_tx(bar_q, kQBytes);
+    for (int kb = 0; kb < 8; ++kb) tma_load_2d(qs + kb * kQBlock, &qmap, bar_q, kb * 64, (int32_t)(row * kH));
+  }
+  griddep_wait();                                              // the selection comes from the previous kernel
+  for (int i = threadIdx.x; i < kMaxTiles * kTile; i += kThreads) {
+    const int j = i / kTile, r = i % kTile;
+    int64_t g = -1;
+    if (j < nt) {
+      if (j < p.win_tiles) {
+        const int64_t c = (int64_t)j * kTile + r;
+        if (c < n_win) g = (int64_t)b * p.N + lo + c;
+      } else {
+        const int64_t slot = (int64_t)(j - p.win_tiles) * kTile + r;
+        int64_t idx = -1;
+        if (p.topk) {
+          if (slot < p.k) idx = p.topk[row * p.k + slot];
+        } else if (slot < V) {
+          idx = slot;
+        }
+        if (idx >= V) { set_error(p.err, DEVERR_BAD_INDEX); idx = -1; }
+        if (idx >= 0) g = (int64_t)b * p.n_cap + idx;
+      }
+    }
+    rows_s[i] = (int32_t)g;
+  }
+  __syncthreads();
+  const uint32_t tmem = *tmem_slot;
+  const int n_loads = 4 * nt;                                  // per phase
+  // load q of phase S: tile q/4, chunk q%4; load q of phase O (half = q / (2 nt)): tile (q % (2 nt)) / 2,
+  // chunk 2 half + q % 2
+  auto load_of = [&](int q, int& j, int& c) {
+    if (q < n_loads) { j = q >> 2; c = q & 3; return; }
+    const int u = q - n_loads, half = u / (2 * nt), v = u % (2 * nt);
+    j = v >> 1;
+    c = 2 * half + (v & 1);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      bool ok = mbar_wait(bar_q, 0, p.err) && mbar_wait(bar_qrot, 0, p.err);
+      const uint32_t q_addr = smem_u32(qs), ring_addr = smem_u32(ring), p_addr = smem_u32(ps);
+      for (int q = 0; q < 2 * n_loads && ok; ++q) {
+        const int st = q % kStages, fill = q / kStages;
+        int j, c;
+        load_of(q, j, c);
+        if (q == n_loads) {                                     // phase O needs P^T
+          mma_commit(bar_s);
+          ok = mbar_wait(bar_p, 0, p.err);
+          if (!ok) break;
+        }
+        if (q == n_loads + 2 * nt) {                            // half 1 reuses the O^T columns
+          mma_commit(bar_o0);
+          ok = mbar_wait(bar_e0, 0, p.err);
+          if (!ok) break;
+        }
+        ok = mbar_wait(&full[st], fill & 1, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t a0 = ring_addr + st * kChunkBytes;
+        if (q < n_loads) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kBlk + (kk & 3) * 32;
+            const uint32_t qoff = (2 * c + (kk >> 2)) * kQBlock + (kk & 3) * 32;
+            mma_bf16(tmem + j * kH, desc_kmajor_sw128(a0 + off), desc_kmajor_sw128(q_addr + qoff), kIdescS,
+                     (c > 0 || kk > 0) ? 1u : 0u);
+          }
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks) {
+            mma_bf16(tmem + kColO + (c & 1) * kH, desc_mnmajor_sw128(a0 + ks * 2048, kBlk),
+                     desc_mnmajor_sw128(p_addr + j * kPBytes + ks * 2048, kBlk), kIdescO,
+                     (j > 0 || ks > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(&empty[st]);
+      }
+      if (ok) mma_commit(bar_o1);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- Q rotation at t
+    bool ok = mbar_wait(bar_q, 0, p.err);
+    if (ok) {
+      rope_line(qs + 7 * kQBlock + lane * 128, lane, t, th_hi, th_lo);
+      rope_line(qs + 7 * kQBlock + (lane + 32) * 128, lane + 32, t, th_hi, th_lo);
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(bar_qrot);
+  } else if (warp >= 6) {
+    // ---------------------------------------------------------------- gather producers
+    const int pt = threadIdx.x - (kThreads - kProducers);     // 0..63
+    bool ok = true;
+    auto issue = [&](int j, int c, int st) {
+      uint8_t* stage = ring + st * kChunkBytes;
+      const __nv_bfloat16* base = j < p.win_tiles ? p.kv : p.ckv;
+#pragma unroll 4
+      for (int i = 0; i < 32; ++i) {
+        const int u = pt + kProducers * i;                     // (row, piece): 16 pieces of 16 B per row
+        const int rr = u >> 4, piece = u & 15;
+        uint8_t* dst = stage + (piece >> 3) * kBlk + sw128_offset(rr, piece & 7);
+        const int32_t g = rows_s[j * kTile + rr];
+        if (g >= 0) cp_async16(dst, base + (int64_t)g * kD + c * 128 + piece * 8);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+      }
+      cp_async_commit();
+    };
+    auto finish = [&](int j, int c, int st) {
+      if (c == 3 && j < p.win_tiles) {                         // raw window rows: RoPE at their positions
+        named_barrier(2, kProducers);
+        for (int rr = pt; rr < kTile; rr += kProducers) {
+          if (rows_s[j * kTile + rr] >= 0)
+            rope_line(ring + st * kChunkBytes + kBlk + rr * 128, rr, lo + (int64_t)j * kTile + rr, th_hi, th_lo);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&full[st]);
+    };
+    for (int q = 0; q < 2 * n_loads; ++q) {
+      const int st = q % kStages, fill = q / kStages;
+      int j, c;
+      load_of(q, j, c);
+      if (fill > 0 && ok) ok = mbar_wait(&empty[st], (fill - 1) & 1, p.err);
+      if (ok) issue(j, c, st);
+      else cp_async_commit();
+      if (q > 0) {
+        int jp, cp;
+        load_of(q - 1, jp, cp);
+        cp_async_wait<1>();
+        finish(jp, cp, (q - 1) % kStages);
+      }
+    }
+    int jl, cl;
+    load_of(2 * n_loads - 1, jl, cl);
+    cp_async_wait<0>();
+    finish(jl, cl, (2 * n_loads - 1) % kStages);
+  } else {
+    // ---------------------------------------------------------------- softmax / epilogue (warps 2..5)
+    const int et = threadIdx.x - 64;                           // 0..127
+    const int wq = warp & 3;
+    const int r = 32 * wq + lane;                              // TMEM lane
+    const int wi = warp - 2;
+    const uint32_t lane_base = tmem + ((wq * 32) << 16);
+    bool ok = mbar_wait(bar_s, 0, p.err);
+    tc_fence_after();
+    float v[64];
+#pragma unroll
+    for (int h = 0; h < 64; ++h) v[h] = -INFINITY;
+    for (int j = 0; j < nt; ++j) {
+      if (!ok || rows_s[j * kTile + r] < 0) continue;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float sv[32];
+        tmem_row32(lane_base + j * kH + half * 32, sv);
+#pragma unroll
+        for (int h = 0; h < 32; ++h) v[half * 32 + h] = fmaxf(v[half * 32 + h], sv[h]);
+      }
+    }
+    reduce_scatter64<true>(v, lane);
+    red[wi * kH + 2 * lane] = v[0];
+    red[wi * kH + 2 * lane + 1] = v[1];
+    named_barrier(1, 128);
+    if (et < kH) {
+      const float m = fmaxf(fmaxf(red[et], red[kH + et]), fmaxf(red[2 * kH + et], red[3 * kH + et]));
+      mx_s[et] = fmaxf(m == -INFINITY ? -INFINITY : m * p.scale, p.sink[et]);   // logit units
+    }
+    named_barrier(1, 128);
+#pragma unroll
+    for (int h = 0; h < 64; ++h) v[h] = 0.f;
+    const float c2 = p.scale * kLog2e;
+    for (int j = 0; j < nt; ++j) {
+      const bool valid = ok && rows_s[j * kTile + r] >= 0;
+      uint8_t* line = ps + j * kPBytes;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float sv[32];
+        if (valid) tmem_row32(lane_base + j * kH + half * 32, sv);
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+          const float e = valid ? exp2f(fmaf(sv[h], c2, -mx_s[half * 32 + h] * kLog2e)) : 0.f;
+          sv[h] = e;
+          v[half * 32 + h] += e;
+        }
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint4 u;
+          u.x = pack_bf16(sv[8 * ch + 0], sv[8 * ch + 1]);
+          u.y = pack_bf16(sv[8 * ch + 2], sv[8 * ch + 3]);
+          u.z = pack_bf16(sv[8 * ch + 4], sv[8 * ch + 5]);
+          u.w = pack_bf16(sv[8 * ch + 6], sv[8 * ch + 7]);
+          *reinterpret_cast<uint4*>(line + sw128_offset(r, half * 4 + ch)) = u;
+        }
+      }
+    }
+    tc_fence_before();
+    fence_proxy_async_smem();
+    mbar_arrive(bar_p);
+    reduce_scatter64<false>(v, lane);
+    red[wi * kH + 2 * lane] = v[0];
+    red[wi * kH + 2 * lane + 1] = v[1];
+    named_barrier(1, 128);
+    if (et < kH) {
+      const float l = (red[et] + red[kH + et]) + (red[2 * kH + et] + red[3 * kH + et]);
+      il_s[et] = 1.f / (l + expf(p.sink[et] - mx_s[et]));
+    }
+    named_barrier(1, 128);
+    // two halves of O^T: thread = dim 128 c + r, 64 heads
+    __nv_bfloat16* orow = p.out + row * kH * kD;
+    for (int half = 0; half < 2; ++half) {
+      if (ok) ok = mbar_wait(half == 0 ? bar_o0 : bar_o1, 0, p.err);
+      tc_fence_after();
+      for (int cc = 0; cc < 2; ++cc) {
+        const int dim = (2 * half + cc) * 128 + r;
+        const bool rot = dim >= kD - p.rope.d_rope;
+        float cs = 1.f, sn = 0.f;
+        if (rot) rope_cs(t, th_hi[(dim - (kD - p.rope.d_rope)) / 2], th_lo[(dim - (kD - p.rope.d_rope)) / 2], cs, sn);
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          float ov[32];
+          if (ok) tmem_row32(lane_base + kColO + cc * kH + hh * 32, ov);
+          else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ov[j] = 0.f;
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int h = hh * 32 + j;
+            float x = ov[j] * il_s[h];
+            if (rot) {                                         // inverse RoPE: the pair partner is lane ^ 1
+              const float y = __shfl_xor_sync(0xffffffffu, x, 1);
+              x = (lane & 1) ? (x * cs - y * sn) : (x * cs + y * sn);
+            }
+            orow[(int64_t)h * kD + dim] = __float2bfloat16_rn(x);
+          }
+        }
+      }
+      if (half == 0) {
+        tc_fence_before();
+        mbar_arrive(bar_e0);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+int tc_attn_prefill_max_tiles() { return kMaxTiles; }
+
+cudaError_t tc_attn_prefill(int B, const AttnParams& a, cudaStream_t st, bool pdl) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int win_tiles = (a.window + kTile - 1) / kTile;
+  const int64_t comp = a.k > 0 ? (a.k + kTile - 1) / kTile : (a.n_cap + kTile - 1) / kTile;
+  if (win_tiles + comp > kMaxTiles) return cudaErrorInvalidValue;
+  if ((int64_t)B * a.N >= (int64_t)1 << 31 || (int64_t)B * a.n_cap >= (int64_t)1 << 31) return cudaErrorInvalidValue;
+  CUtensorMap qmap;
+  cudaError_t e = make_tmap_2d(&qmap, a.q, (int64_t)B * a.S * kH, kD, kH);
+  if (e != cudaSuccess) return e;
+  PrefillParams p;
+  p.kv = static_cast<const __nv_bfloat16*>(a.kv);
+  p.ckv = static_cast<const __nv_bfloat16*>(a.ckv);
+  p.topk = a.topk; p.pos = a.pos; p.sink = a.sink; p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.N = a.N; p.n_cap = a.n_cap; p.S = a.S; p.k = a.k; p.ratio = a.ratio; p.window = a.window;
+  p.win_tiles = win_tiles; p.n_tiles = win_tiles + (int)comp; p.scale = a.scale; p.rope = a.rope; p.err = a.err;
+  dim3 grid((unsigned)a.S, (unsigned)B);
+  return launch_kernel(pdl, attn_prefill_kernel, grid, dim3(kThreads), kSmemBytes, st, qmap, p);
+}
+
+}  // namespace csa

@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
   float* w_s = reinterpret_cast<float*>(tmem_slot + 4);    // [64]
 
+  griddep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z, s = blockIdx.y;
   const int64_t row = (int64_t)b * p.S + s;
@@ -91,6 +92,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       prefetch_tensormap(&cmap);
+      griddep_wait();                                       // the cache may come from the previous kernel
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages;
         if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1, p.err)) break;
@@ -127,18 +129,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int et = threadIdx.x - 64;                        // 0..127
     const __nv_bfloat16* q = p.q_idx + row * 64 * kDI;
     const int r0 = kDI - p.rope.d_rope;
-    for (int u = et; u < 64 * (kDI / 8); u += 128) {        // (head, 8-dim chunk)
-      const int h = u / (kDI / 8), c = u % (kDI / 8);
-      float x[8];
-      load8(q + h * kDI + c * 8, x);
-      if (c * 8 >= r0) {
+    // thread et owns the 8-dim chunk c = et % 16 of heads et/16 + 8 i, i < 8: all loads first
+    const int c = et % (kDI / 8), h0 = et / (kDI / 8);
+    float xs[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) load8(q + (h0 + 8 * i) * kDI + c * 8, xs[i]);
+    const float wv = et < 64 ? p.w[row * 64 + et] : 0.f;
+    float cs4[4], sn4[4];
+    const bool rot = c * 8 >= r0;
+    if (rot) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) rope_cs(t, p.rope, (c * 8 - r0) / 2 + k, cs4[k], sn4[k]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float* x = xs[i];
+      if (rot) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          float cs, sn;
-          rope_cs(t, p.rope, (c * 8 - r0) / 2 + k, cs, sn);
           const float a = x[2 * k], bb = x[2 * k + 1];
-          x[2 * k] = a * cs - bb * sn;
-          x[2 * k + 1] = a * sn + bb * cs;
+          x[2 * k] = a * cs4[k] - bb * sn4[k];
+          x[2 * k + 1] = a * sn4[k] + bb * cs4[k];
         }
       }
       float hi[8], lo[8];
@@ -147,17 +158,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         hi[k] = __bfloat162float(__float2bfloat16_rn(x[k]));
         lo[k] = x[k] - hi[k];
       }
-      const int blk = c >> 3, ch = c & 7;
+      const int h = h0 + 8 * i, blk = c >> 3, ch = c & 7;
       store8(reinterpret_cast<__nv_bfloat16*>(qop + blk * kBlockBytes + sw128_offset(h, ch)), hi);
       store8(reinterpret_cast<__nv_bfloat16*>(qop + blk * kBlockBytes + sw128_offset(64 + h, ch)), lo);
     }
-    if (et < 64) w_s[et] = p.w[row * 64 + et];
+    if (et < 64) w_s[et] = wv;
     fence_proxy_async_smem();
     mbar_arrive(qready);
     named_barrier(1, 128);                                  // w_s visible to every epilogue thread
 
     const uint32_t quad = warp & 3;                         // TMEM lanes 32*quad .. 32*quad+31
     float* out = p.scores + row * p.n_cap;
+    griddep_wait();
     for (int i = 0; i < ntiles; ++i) {
       const int acc = i & 1;
       if (!mbar_wait(&tfull[acc], (i >> 1) & 1, p.err)) break;
@@ -232,7 +244,7 @@ int tc_sm_count() {
 
 cudaError_t tc_index_scores(int B, int S, const int64_t* pos, const void* q_idx, const float* w, const void* cidx,
                             int64_t n_cap, int ratio, const RopeTab& rope, float* scores, void*, int32_t* err,
-                            cudaStream_t st) {
+                            cudaStream_t st, bool pdl) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(index_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
@@ -252,8 +264,7 @@ cudaError_t tc_index_scores(int B, int S, const int64_t* pos, const void* q_idx,
   if (chunks > tiles) chunks = tiles;
   p.chunks = (int)chunks;
   dim3 grid((unsigned)chunks, (unsigned)S, (unsigned)B);
-  index_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(map, p);
-  return cudaGetLastError();
+  return launch_kernel(pdl, index_tc_kernel, grid, dim3(kThreads), kSmemBytes, st, map, p);
 }
 
 }  // namespace csa

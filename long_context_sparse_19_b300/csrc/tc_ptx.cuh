@@ -168,5 +168,62 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
+// ------------------------------------------------------------------ attention helpers
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// rotate the 32 interleaved pairs of one 128-byte swizzled line (dims 448..511) by angle pos*theta_i
+__device__ __forceinline__ void rope_line(uint8_t* line_base, uint32_t row, int64_t pos, const float* th_hi,
+                                          const float* th_lo) {
+#pragma unroll 2
+  for (int ch = 0; ch < 8; ++ch) {
+    uint4* p = reinterpret_cast<uint4*>(line_base + ((ch ^ (row & 7u)) << 4));
+    uint4 u = *p;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float c, s;
+      rope_cs(pos, th_hi[ch * 4 + k], th_lo[ch * 4 + k], c, s);
+      const float a = bf16lo(w[k]), b = bf16hi(w[k]);
+      w[k] = pack_bf16(a * c - b * s, a * s + b * c);
+    }
+    *p = u;
+  }
+}
+
+// butterfly reduce-scatter of 64 per-lane values over the 32 lanes: afterwards lane l holds the
+// reduction of heads 2l and 2l+1 in v[0], v[1].
+template <bool kMax>
+__device__ __forceinline__ void reduce_scatter64(float (&v)[64], int lane) {
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int half = 32 >> step;
+    const int bit = 16 >> step;
+    const bool upper = (lane & bit) != 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j < half) {
+        const float keep = upper ? v[j + half] : v[j];
+        const float send = upper ? v[j] : v[j + half];
+        const float got = __shfl_xor_sync(0xffffffffu, send, bit);
+        v[j] = kMax ? fmaxf(keep, got) : keep + got;
+      }
+    }
+  }
+}
+
+// 32 TMEM columns of this warp's lane quadrant as floats
+__device__ __forceinline__ void tmem_row32(uint32_t taddr, float (&v)[32]) {
+  uint32_t u[32];
+  tmem_ld32(taddr, u);
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(u[j]);
+}
+
 }  // namespace tc
 }  // namespace csa

@@ -99,9 +99,12 @@ def check_scores(got: np.ndarray, ref: np.ndarray, storage: str, what: str):
 
 
 def check_topk_exact(got: np.ndarray, scores: np.ndarray, k: int, what: str):
-    """The GPU selection equals the exact selection on the same float32 scores."""
+    """The GPU selection equals the exact (-score, index) selection on the same float32 scores,
+    listed in ascending entry index with -1 in the unused slots."""
     want = O.topk_select(scores, k)
-    assert np.array_equal(got, want), f"{what}: top-k differs from the exact selection on its scores"
+    n = int((want >= 0).sum())
+    exp = np.concatenate([np.sort(want[:n]), np.full(k - n, -1, dtype=want.dtype)])
+    assert np.array_equal(got, exp), f"{what}: top-k differs from the exact selection on its scores"
 
 
 def check_topk_vs_oracle(got: np.ndarray, ref_scores: np.ndarray, k: int, what: str):

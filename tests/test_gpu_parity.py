@@ -18,6 +18,11 @@ DECODE = {
     "hca_bf16": (synth.small_workload(3, wid=103, B=2, N=8256, t=8255), [8255, 5000]),
     "csa_f32": (synth.small_workload(0, wid=100, B=2), [2047, 1001]),
     "csa_f32_cfg0": (synth.WORKLOADS[0], [2047]),
+    # enough rows that the tensor-core attention puts two candidate tiles in one CTA
+    "csa_bf16_B32": (synth.small_workload(1, wid=104, B=32, N=4099, t=4098),
+                     [4098 - 37 * b for b in range(32)]),
+    "hca_bf16_B16_wide": (synth.small_workload(3, wid=105, B=16, N=19215, t=19214, ratio=16),
+                          [19214, 19199] + [19214 - 977 * b for b in range(2, 16)]),
 }
 MODES = [False, True]          # tensor-core path where available, then the CUDA-core path
 
@@ -255,3 +260,40 @@ def test_argument_errors_launch_nothing():
                      bt.sink, out, ws=ws)
     assert e.value.status == 4
     assert torch.all(out == 0)
+
+
+@pytest.mark.parametrize("n_cap,k,B,dup", [
+    (20000, 512, 2, False),      # two chunks, then a candidate level
+    (262144, 512, 1, False),     # the 1M-token workload's row length: sixteen chunks
+    (70000, 2048, 1, True),      # k = 2048 with exact ties (repeated cache rows): three levels
+    (5000, 2048, 1, False),      # fewer visible entries than k: everything, sorted, -1 tail
+])
+def test_topk_long_rows_exact(n_cap, k, B, dup):
+    """Indexer + selection on rows longer than one CTA holds: the GPU's selection equals the exact
+    (-score, index) selection of its own scores; the scores match the oracle."""
+    rng = np.random.default_rng(n_cap + k)
+    import synth as S
+    L = Hn.lib()
+    H_idx = 64
+    cidx = S.round_bf16(rng.standard_normal((B, n_cap, 128), dtype=np.float32) / np.float32(np.sqrt(128)))
+    if dup:
+        cidx[:, 3000:] = cidx[:, np.arange(3000, n_cap) % 3000]
+    q_idx = S.round_bf16(rng.standard_normal((B, 1, H_idx, 128), dtype=np.float32) / np.float32(np.sqrt(128)))
+    w = (rng.standard_normal((B, 1, H_idx)) / np.sqrt(128 * H_idx)).astype(np.float32)
+    c = L.Config(top_k=k, ratio=4)
+    pos = np.array([[4 * n_cap - 1]] * B, np.int64)
+    if B > 1:
+        pos[1, 0] = 4 * (n_cap - 777) - 2          # fewer visible entries in the second row
+    d_cidx, d_q = Hn.dev(cidx, "bf16"), Hn.dev(q_idx, "bf16")
+    topk = torch.empty(B, 1, k, dtype=torch.int32, device="cuda")
+    scores = torch.full((B, 1, n_cap), float("nan"), device="cuda")
+    L.csa_index_topk(c, torch.from_numpy(pos).cuda(), d_q, torch.from_numpy(w).cuda(), d_cidx, topk, scores)
+    torch.cuda.synchronize()
+    for b in range(B):
+        t = int(pos[b, 0])
+        V = O.visible(t, 4)
+        got = scores[b, 0, :V].double().cpu().numpy()
+        tk = topk[b, 0].cpu().numpy()
+        Hn.check_topk_exact(tk, got, k, f"long row b{b}")
+        ref = O.index_scores(q_idx[b, 0], w[b, 0], cidx[b], t, 4)
+        Hn.check_scores(got, ref, "bf16", f"long row scores b{b}")
