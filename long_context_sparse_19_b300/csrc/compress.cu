@@ -16,7 +16,7 @@ namespace csa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kEntriesPerBlock = 64;
+constexpr int kEntriesPerBlock = 64;   // large builds; small ones use 16 so that the grid fills the GPU
 
 struct Stat8 {
   float mx[8], sum[8], acc[8];
@@ -132,8 +132,8 @@ __device__ void compress_block(const CompressParams& p, const CompressJob& job, 
   const int team = threadIdx.x / TPE;
   const int tt = threadIdx.x % TPE;
   const int b = blockIdx.y;
-  constexpr int EPT = kEntriesPerBlock / TEAMS;
-  const int64_t e_begin = p.first_entry + (int64_t)blockIdx.x * kEntriesPerBlock + (int64_t)team * EPT;
+  const int EPT = p.epb / TEAMS;                  // entries per team (epb is a multiple of 16)
+  const int64_t e_begin = p.first_entry + (int64_t)blockIdx.x * p.epb + (int64_t)team * EPT;
   const int64_t e_end = min(e_begin + EPT, p.first_entry + p.n_entries);
   if (e_begin >= e_end) return;
   compress_run<T, C>(p, job, b, e_begin, e_end, team, tt, red);
@@ -283,11 +283,14 @@ cudaError_t launch_compress(bool bf16, int B, const CompressParams& p, cudaStrea
     }
     return e;
   }
-  const int64_t nb = (p.n_entries + kEntriesPerBlock - 1) / kEntriesPerBlock;
+  CompressParams q = p;
+  q.epb = kEntriesPerBlock;
+  if ((p.n_entries + kEntriesPerBlock - 1) / kEntriesPerBlock * B * p.n_jobs < 4 * 148) q.epb = 16;
+  const int64_t nb = (p.n_entries + q.epb - 1) / q.epb;
   if (nb == 0) return cudaSuccess;
   dim3 grid((unsigned)nb, (unsigned)B, (unsigned)p.n_jobs);
-  if (bf16) return launch_kernel(pdl, compress_kernel<__nv_bfloat16>, grid, dim3(kThreads), 0, st, p);
-  return launch_kernel(pdl, compress_kernel<float>, grid, dim3(kThreads), 0, st, p);
+  if (bf16) return launch_kernel(pdl, compress_kernel<__nv_bfloat16>, grid, dim3(kThreads), 0, st, q);
+  return launch_kernel(pdl, compress_kernel<float>, grid, dim3(kThreads), 0, st, q);
 }
 
 }  // namespace csa

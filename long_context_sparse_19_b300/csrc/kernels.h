@@ -21,6 +21,7 @@ struct CompressParams {
   int64_t first_entry, n_entries;   // range mode
   const int64_t* pos;    // close mode when non-null: entry pos[b]/m if (pos[b]+1) % m == 0
   int ratio;
+  int epb;               // range mode: entries per CTA (set by the launcher)
   float eps;
   RopeTab rope;
   int32_t* err;

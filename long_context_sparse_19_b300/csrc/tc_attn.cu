@@ -259,20 +259,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     finish((n_loads_s - 1) / 4, (n_loads_s - 1) % 4, (n_loads_s - 1) % kStages);
 
     // ---------------------------------------------------------------- softmax over the CTA's candidates
-    if (ok) ok = mbar_wait(bar_s, 0, p.err);
+    // TMEM loads are warp-collective: every lane loads, empty rows are masked afterwards
+    ok = mbar_wait_warp(bar_s, 0, p.err) && __all_sync(0xffffffffu, ok);
     tc_fence_after();
     const uint32_t lane_base = tmem + ((wq * 32) << 16);
     float v[64];
 #pragma unroll
     for (int h = 0; h < 64; ++h) v[h] = -INFINITY;
-    for (int j = 0; j < nt; ++j) {
-      if (!ok || rows_s[j * kTile + r] < 0) continue;
+    for (int j = 0; j < nt && ok; ++j) {
+      const bool valid = rows_s[j * kTile + r] >= 0;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float sv[32];
         tmem_row32(lane_base + j * kH + half * 32, sv);
 #pragma unroll
-        for (int h = 0; h < 32; ++h) v[half * 32 + h] = fmaxf(v[half * 32 + h], sv[h]);
+        for (int h = 0; h < 32; ++h) v[half * 32 + h] = fmaxf(v[half * 32 + h], valid ? sv[h] : -INFINITY);
       }
     }
     const int wi = warp - 2;
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float sv[32];
-        if (valid) tmem_row32(lane_base + j * kH + half * 32, sv);
+        if (ok) tmem_row32(lane_base + j * kH + half * 32, sv);     // ok is warp-uniform
 #pragma unroll
         for (int h = 0; h < 32; ++h) {
           const float m = m_s[half * 32 + h];
@@ -336,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       p.part_ml[2 * (pi + pt) + 1] = l;
     }
     // split partial O: thread = dim 128 dc + r, 64 heads
-    if (ok) ok = mbar_wait(bar_o, 0, p.err);
+    ok = mbar_wait_warp(bar_o, 0, p.err) && __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after();
 #pragma unroll 1

@@ -262,19 +262,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = 32 * wq + lane;                              // TMEM lane
     const int wi = warp - 2;
     const uint32_t lane_base = tmem + ((wq * 32) << 16);
-    bool ok = mbar_wait(bar_s, 0, p.err);
+    // TMEM loads are warp-collective: every lane loads, empty rows are masked afterwards
+    bool ok = mbar_wait_warp(bar_s, 0, p.err);
     tc_fence_after();
     float v[64];
 #pragma unroll
     for (int h = 0; h < 64; ++h) v[h] = -INFINITY;
-    for (int j = 0; j < nt; ++j) {
-      if (!ok || rows_s[j * kTile + r] < 0) continue;
+    for (int j = 0; j < nt && ok; ++j) {
+      const bool valid = rows_s[j * kTile + r] >= 0;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float sv[32];
         tmem_row32(lane_base + j * kH + half * 32, sv);
 #pragma unroll
-        for (int h = 0; h < 32; ++h) v[half * 32 + h] = fmaxf(v[half * 32 + h], sv[h]);
+        for (int h = 0; h < 32; ++h) v[half * 32 + h] = fmaxf(v[half * 32 + h], valid ? sv[h] : -INFINITY);
       }
     }
     reduce_scatter64<true>(v, lane);
@@ -295,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float sv[32];
-        if (valid) tmem_row32(lane_base + j * kH + half * 32, sv);
+        if (ok) tmem_row32(lane_base + j * kH + half * 32, sv);     // ok is warp-uniform
 #pragma unroll
         for (int h = 0; h < 32; ++h) {
           const float e = valid ? exp2f(fmaf(sv[h], c2, -mx_s[half * 32 + h] * kLog2e)) : 0.f;
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // two halves of O^T: thread = dim 128 c + r, 64 heads
     __nv_bfloat16* orow = p.out + row * kH * kD;
     for (int half = 0; half < 2; ++half) {
-      if (ok) ok = mbar_wait(half == 0 ? bar_o0 : bar_o1, 0, p.err);
+      ok = mbar_wait_warp(half == 0 ? bar_o0 : bar_o1, 0, p.err) && ok;
       tc_fence_after();
       for (int cc = 0; cc < 2; ++cc) {
         const int dim = (2 * half + cc) * 128 + r;

@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     griddep_wait();
     for (int i = 0; i < ntiles; ++i) {
       const int acc = i & 1;
-      if (!mbar_wait(&tfull[acc], (i >> 1) & 1, p.err)) break;
+      if (!mbar_wait_warp(&tfull[acc], (i >> 1) & 1, p.err)) break;    // uniform over the warp
       tc_fence_after();
       const uint32_t ta = tmem + ((quad * 32) << 16) + acc * 128;
       float sc = 0.f;
