@@ -170,6 +170,34 @@ csa_status csa_prefill(const csa_config* cfg, int32_t B, int32_t S, const csa_ca
                        void* out, int32_t* topk_out, void* ws, size_t ws_bytes,
                        cudaStream_t stream);
 
+/* ---- For callers that cannot allocate device memory ------------------------------------------
+ * The source pages have no counterpart of this call: it is a deployment convenience of the
+ * library, computing exactly what csa_index_topk computes.
+ *
+ * csa_index_topk needs a caller workspace. Some callers have no way to provide one: an engine
+ * whose device memory was reserved up front by another allocator has none left to hand out, a
+ * latency-critical serving loop must not call cudaMalloc / cudaFree (they can synchronise the
+ * device and take unbounded time), and some plugin hosts do not let a library allocate at all.
+ * csa_index_topk_static takes the arguments of csa_index_topk minus (ws, ws_bytes) and allocates
+ * nothing: its temporary buffers (the float32 scores when `scores` is NULL, the selection, and the
+ * candidate lists of rows longer than 16,384 entries) live in one fixed device array of
+ * CSA_STATIC_SCRATCH_BYTES inside this library. Every device that loads the library holds that
+ * array until the process exits.
+ *  - Limit: a request whose temporary buffers exceed CSA_STATIC_SCRATCH_BYTES (about
+ *    4 * B * S * n_cap bytes of scores plus the selections) is rejected with CSA_ERR_WORKSPACE
+ *    before anything is launched; use csa_index_topk with a workspace for it.
+ *  - Set-up: the first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current. Make that first call before any stream
+ *    capture begins.
+ *  - Sharing: every call uses the same array and leaves its contents there; nothing in it has to
+ *    start at zero (a call writes every byte it later reads). Calls that can overlap on the GPU
+ *    (other streams, other host threads) race on the array: the caller must serialise them.
+ * Arguments, results and other errors are those of csa_index_topk. */
+#define CSA_STATIC_SCRATCH_BYTES (8u << 20)
+csa_status csa_index_topk_static(const csa_config* cfg, int32_t B, int32_t S, const int64_t* pos,
+                                 const void* q_idx, const float* w, const void* cidx, int64_t n_cap,
+                                 int32_t* topk, float* scores, cudaStream_t stream);
+
 /* ---- Instrumentation (host side; never changes results) -------------------------------------
  * Stage ids used below: 0 compressor, 1 indexer scores, 2 top-k, 3 sparse attention, 4 split merge. */
 

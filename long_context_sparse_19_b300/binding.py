@@ -21,7 +21,8 @@ CSA_FLAG_SIMT = 1
 
 # the public entry points declared in include/csa.h
 EXPORTS = ("csa_status_string", "csa_last_error", "csa_get_device_status", "csa_workspace_bytes",
-           "csa_compress", "csa_index_topk", "csa_sparse_attn", "csa_decode", "csa_prefill",
+           "csa_compress", "csa_index_topk", "csa_index_topk_static", "csa_sparse_attn", "csa_decode",
+           "csa_prefill",
            "csa_launch_count", "csa_profile_begin", "csa_profile_end")
 STAGES = ("compress", "index", "topk", "attn", "merge")
 
@@ -64,6 +65,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.csa_compress.argtypes, L.csa_compress.restype = [cp, c_int32, POINTER(CsaCache), c_int64, c_int64, vp], c_int
     L.csa_index_topk.argtypes = [cp, c_int32, c_int32, vp, vp, vp, vp, c_int64, vp, vp, vp, c_size_t, vp]
     L.csa_index_topk.restype = c_int
+    L.csa_index_topk_static.argtypes = [cp, c_int32, c_int32, vp, vp, vp, vp, c_int64, vp, vp, vp]
+    L.csa_index_topk_static.restype = c_int
     L.csa_sparse_attn.argtypes = [cp, c_int32, c_int32, vp, vp, vp, c_int64, vp, c_int64, vp, vp, vp, vp,
                                   c_size_t, vp]
     L.csa_sparse_attn.restype = c_int
@@ -200,6 +203,19 @@ def csa_index_topk(cfg: Config, pos, q_idx, w, cidx, topk, scores=None, ws=None,
         _ptr(cidx, (B, n_cap, cfg.d_idx), cfg.dtype, "cidx"), n_cap,
         _ptr(topk, (B, S, cfg.top_k), torch.int32, "topk"), _ptr(scores, (B, S, n_cap), torch.float32, "scores"),
         _ptr(ws, None, torch.uint8, "ws"), ws.numel(), _stream(stream)), "csa_index_topk")
+
+
+def csa_index_topk_static(cfg: Config, pos, q_idx, w, cidx, topk, scores=None, stream=None) -> None:
+    """csa_index_topk without a workspace: the library's fixed device scratch array is used instead
+    (nothing is allocated; see include/csa.h for the size limit and the sharing rules)."""
+    B, S = pos.shape
+    n_cap = cidx.shape[1]
+    _check(load().csa_index_topk_static(
+        ctypes.byref(cfg.c()), B, S, _ptr(pos, (B, S), torch.int64, "pos"),
+        _ptr(q_idx, (B, S, cfg.H_idx, cfg.d_idx), cfg.dtype, "q_idx"), _ptr(w, (B, S, cfg.H_idx), torch.float32, "w"),
+        _ptr(cidx, (B, n_cap, cfg.d_idx), cfg.dtype, "cidx"), n_cap,
+        _ptr(topk, (B, S, cfg.top_k), torch.int32, "topk"), _ptr(scores, (B, S, n_cap), torch.float32, "scores"),
+        _stream(stream)), "csa_index_topk_static")
 
 
 def csa_sparse_attn(cfg: Config, pos, q, kv, ckv, topk, sink, out, ws=None, stream=None) -> None:

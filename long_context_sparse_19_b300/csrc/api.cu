@@ -36,6 +36,29 @@ int32_t* device_error_word() {
   return addr[dev];
 }
 
+// Scratch of csa_index_topk_static: one fixed device array (every device that loads the library
+// holds it until the process exits); no call ever allocates it or frees it.
+__device__ __align__(256) uint8_t g_static_scratch[CSA_STATIC_SCRATCH_BYTES];
+
+// Device address of g_static_scratch on the current device, looked up once per device with that
+// device current (host code must not pass the symbol itself to a kernel).
+uint8_t* static_scratch(cudaError_t* err) {
+  static std::mutex mu;
+  static uint8_t* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess && (dev < 0 || dev >= 64)) e = cudaErrorInvalidDevice;
+  if (e != cudaSuccess) { *err = e; return nullptr; }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess) { *err = e; return nullptr; }
+    addr[dev] = static_cast<uint8_t*>(ptr);
+  }
+  return addr[dev];
+}
+
 csa_status fail(csa_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 csa_status fail(csa_status s, const char* fmt, ...) {
   char buf[512];
@@ -370,6 +393,31 @@ csa_status csa_index_topk(const csa_config* cfg, int32_t B, int32_t S, const int
   float* sc = scores ? scores : carve<float>(ws, pl.off_scores);
   return run_index_topk(cfg, B, S, pos, q_idx, w, cidx, n_cap, topk, sc, carve<char>(ws, pl.off_tksel),
                         carve<char>(ws, pl.off_tc), stream, false);
+}
+
+csa_status csa_index_topk_static(const csa_config* cfg, int32_t B, int32_t S, const int64_t* pos,
+                                 const void* q_idx, const float* w, const void* cidx, int64_t n_cap,
+                                 int32_t* topk, float* scores, cudaStream_t stream) {
+  csa_status s = check_config(cfg);
+  if (s != CSA_OK) return s;
+  if (cfg->top_k == 0) return fail(CSA_ERR_INVALID_ARG, "top_k == 0 (HCA) has no indexer");
+  if (B < 0 || B > 65535 || S < 0 || S > 65535) return fail(CSA_ERR_SHAPE, "B = %d, S = %d", B, S);
+  if (n_cap < 1) return fail(CSA_ERR_SHAPE, "n_cap = %lld", (long long)n_cap);
+  CHECK_PTR(pos); CHECK_PTR(q_idx); CHECK_PTR(w); CHECK_PTR(cidx); CHECK_PTR(topk); CHECK_OPT_PTR(scores);
+  // the indexer and selection use the front of the workspace plan: scores, selection, candidates
+  const Plan pl = make_plan(cfg, B, S, n_cap);
+  const size_t need = pl.off_tksel + topk_workspace_bytes((int64_t)B * S, n_cap, cfg->top_k);
+  if (need > (size_t)CSA_STATIC_SCRATCH_BYTES)
+    return fail(CSA_ERR_WORKSPACE,
+                "csa_index_topk_static: B = %d, S = %d, n_cap = %lld need %zu bytes of scratch, more than the "
+                "static %u-byte array; call csa_index_topk with a workspace instead",
+                B, S, (long long)n_cap, need, (unsigned)CSA_STATIC_SCRATCH_BYTES);
+  cudaError_t e = cudaSuccess;
+  uint8_t* ws = static_scratch(&e);
+  if (!ws) return cuda_status(e, "csa_index_topk_static: device address of the static scratch");
+  if (B == 0 || S == 0) return CSA_OK;
+  float* sc = scores ? scores : reinterpret_cast<float*>(ws + pl.off_scores);
+  return run_index_topk(cfg, B, S, pos, q_idx, w, cidx, n_cap, topk, sc, ws + pl.off_tksel, nullptr, stream, false);
 }
 
 csa_status csa_sparse_attn(const csa_config* cfg, int32_t B, int32_t S, const int64_t* pos, const void* q,
