@@ -200,9 +200,11 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnParams p)
 
 // Merge of split partials: M = max(m_i, sink), L = sum_i l_i e^(m_i - M) + e^(sink - M),
 // o = sum_i e^(m_i - M) o_i / L, then the inverse RoPE at t. One CTA per (query, 8 heads): warp w
-// owns head 8 blockIdx.x + w, lane l owns dims 16 l .. 16 l + 15 (four float4 per split); the
-// split weights are computed lane-parallel and broadcast with shuffles.
+// owns head 8 blockIdx.x + w, lane l owns dims 16 l .. 16 l + 15. The split statistics (lane i
+// holds split i) and the partial outputs of up to kMergeBatch splits are loaded in one round, so
+// the kernel pays the L2 latency once per batch instead of once per dependent step.
 constexpr int kMergeHeads = 8;
+constexpr int kMergeBatch = 4;
 
 template <typename T>
 __global__ void __launch_bounds__(32 * kMergeHeads) attn_merge_kernel(const AttnParams p) {
@@ -217,41 +219,54 @@ __global__ void __launch_bounds__(32 * kMergeHeads) attn_merge_kernel(const Attn
   const float sk = p.sink[h];
   const float* ml = p.part_ml + (row * p.n_split * p.H + h) * 2;     // split i at ml[2 * i * H]
   const int64_t mstride = 2 * (int64_t)p.H;
-  float M = sk;
-  for (int i = lane; i < p.n_split; i += 32) M = fmaxf(M, ml[i * mstride]);
-  M = warp_max(M);
-  float L = 0.f;
-  for (int i = lane; i < p.n_split; i += 32) {
-    const float mi = ml[i * mstride];
-    if (mi != -INFINITY) L = fmaf(ml[i * mstride + 1], expf(mi - M), L);
-  }
-  L = warp_sum(L) + expf(sk - M);
-  float acc[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
   const int d0 = lane * 16;
   const float* po = p.part_o + (row * p.n_split * p.H + h) * kD + d0;
   const int64_t ostride = (int64_t)p.H * kD;
+  // the first batch of partial outputs is requested together with the split statistics
+  float4 v[kMergeBatch][4];
+  auto load_batch = [&](int first) {
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      if (first + u < p.n_split) {
+        const float4* src = reinterpret_cast<const float4*>(po + (int64_t)(first + u) * ostride);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[u][q] = src[q];
+      }
+    }
+  };
+  load_batch(0);
+  float M = sk;
+  for (int i = lane; i < p.n_split; i += 32) M = fmaxf(M, ml[i * mstride]);
+  M = warp_max(M);
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  float L = 0.f;
   for (int i0 = 0; i0 < p.n_split; i0 += 32) {
     const int i = i0 + lane;
-    const float mi = i < p.n_split ? ml[i * mstride] : -INFINITY;
+    float mi = -INFINITY, li = 0.f;
+    if (i < p.n_split) { mi = ml[i * mstride]; li = ml[i * mstride + 1]; }
     const float wgt = mi == -INFINITY ? 0.f : expf(mi - M);
+    L = fmaf(li, wgt, L);
     const int cnt = min(32, p.n_split - i0);
-#pragma unroll 2
-    for (int u = 0; u < cnt; ++u) {
-      const float a = __shfl_sync(0xffffffffu, wgt, u);
-      if (a == 0.f) continue;
-      const float4* src = reinterpret_cast<const float4*>(po + (int64_t)(i0 + u) * ostride);
+    for (int u0 = 0; u0 < cnt; u0 += kMergeBatch) {
+      if (i0 + u0 > 0) load_batch(i0 + u0);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 v = src[q];
-        acc[4 * q + 0] = fmaf(a, v.x, acc[4 * q + 0]);
-        acc[4 * q + 1] = fmaf(a, v.y, acc[4 * q + 1]);
-        acc[4 * q + 2] = fmaf(a, v.z, acc[4 * q + 2]);
-        acc[4 * q + 3] = fmaf(a, v.w, acc[4 * q + 3]);
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const float a = __shfl_sync(0xffffffffu, wgt, (u0 + u) & 31);
+        if (u0 + u < cnt && a != 0.f) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            acc[4 * q + 0] = fmaf(a, v[u][q].x, acc[4 * q + 0]);
+            acc[4 * q + 1] = fmaf(a, v[u][q].y, acc[4 * q + 1]);
+            acc[4 * q + 2] = fmaf(a, v[u][q].z, acc[4 * q + 2]);
+            acc[4 * q + 3] = fmaf(a, v[u][q].w, acc[4 * q + 3]);
+          }
+        }
       }
     }
   }
+  L = warp_sum(L) + expf(sk - M);
   const float inv = 1.f / L;
 #pragma unroll
   for (int k = 0; k < 16; ++k) acc[k] *= inv;

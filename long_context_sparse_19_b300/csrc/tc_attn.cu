@@ -244,19 +244,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(&full[st]);
     };
-    // S^T phase loads: q -> (tile q/4, chunk q%4), stage q%4, fill q/4
+    // S^T phase loads: q -> (tile q/4, chunk q%4), stage q%4, fill q/4; up to kStages - 1 loads stay
+    // in flight while the oldest one is completed
     for (int q = 0; q < n_loads_s; ++q) {
       const int st = q % kStages, fill = q / kStages;
       if (fill > 0 && ok) ok = mbar_wait(&empty[st], (fill - 1) & 1, p.err);
       if (ok) issue(q / 4, q % 4, st);
       else cp_async_commit();
-      if (q > 0) {
-        cp_async_wait<1>();
-        finish((q - 1) / 4, (q - 1) % 4, (q - 1) % kStages);
+      if (q >= kStages - 1) {
+        cp_async_wait<kStages - 1>();
+        const int d = q - (kStages - 1);
+        finish(d / 4, d % 4, d % kStages);
       }
     }
     cp_async_wait<0>();
-    finish((n_loads_s - 1) / 4, (n_loads_s - 1) % 4, (n_loads_s - 1) % kStages);
+    for (int d = n_loads_s - (kStages - 1) > 0 ? n_loads_s - (kStages - 1) : 0; d < n_loads_s; ++d)
+      finish(d / 4, d % 4, d % kStages);
 
     // ---------------------------------------------------------------- softmax over the CTA's candidates
     // TMEM loads are warp-collective: every lane loads, empty rows are masked afterwards
@@ -321,10 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = mbar_wait(&empty[c], 1, p.err);
         if (ok) issue(0, c, c);
         else cp_async_commit();
-        if (c > 0) { cp_async_wait<1>(); finish(0, c - 1, c - 1); }
       }
-      cp_async_wait<0>();
-      finish(0, 3, 3);
+      cp_async_wait<3>(); finish(0, 0, 0);
+      cp_async_wait<2>(); finish(0, 1, 1);
+      cp_async_wait<1>(); finish(0, 2, 2);
+      cp_async_wait<0>(); finish(0, 3, 3);
     }
     reduce_scatter64<false>(v, lane);
     red[wi * kH + 2 * lane] = v[0];

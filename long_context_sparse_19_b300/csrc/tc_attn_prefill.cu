@@ -244,17 +244,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (fill > 0 && ok) ok = mbar_wait(&empty[st], (fill - 1) & 1, p.err);
       if (ok) issue(j, c, st);
       else cp_async_commit();
-      if (q > 0) {
+      if (q >= kStages - 1) {                                  // up to kStages - 1 loads in flight
+        const int d = q - (kStages - 1);
         int jp, cp;
-        load_of(q - 1, jp, cp);
-        cp_async_wait<1>();
-        finish(jp, cp, (q - 1) % kStages);
+        load_of(d, jp, cp);
+        cp_async_wait<kStages - 1>();
+        finish(jp, cp, d % kStages);
       }
     }
-    int jl, cl;
-    load_of(2 * n_loads - 1, jl, cl);
     cp_async_wait<0>();
-    finish(jl, cl, (2 * n_loads - 1) % kStages);
+    for (int d = 2 * n_loads - (kStages - 1) > 0 ? 2 * n_loads - (kStages - 1) : 0; d < 2 * n_loads; ++d) {
+      int jl, cl;
+      load_of(d, jl, cl);
+      finish(jl, cl, d % kStages);
+    }
   } else {
     // ---------------------------------------------------------------- softmax / epilogue (warps 2..5)
     const int et = threadIdx.x - 64;                           // 0..127

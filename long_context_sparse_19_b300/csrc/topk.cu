@@ -323,17 +323,20 @@ cudaError_t launch_select(const SelParams& p, int64_t rows, int cap, cudaStream_
   return launch_kernel(pdl, topk_select_kernel<kThreads>, grid, dim3(kThreads), smem, st, p, cap);
 }
 
-// Items one CTA holds: the large variant (1024 threads) serves long rows, the small one (256
-// threads, several CTAs per SM) the many short rows of a prefill.
+// Items one CTA holds: the large variant (1024 threads) serves the later levels of very long rows;
+// the small one (512 threads for decode rows, 256 for the many short rows of a prefill) the first
+// level and every short row. Cutting decode rows into 4096-entry chunks spreads the first level
+// over many SMs; its winners (k per chunk) are then few enough for one small CTA per row.
 constexpr int kCapLarge = 16384;
 constexpr int kCapSmall = 4096;
 
 }  // namespace
 
 size_t topk_workspace_bytes(int64_t rows, int64_t n_cap, int k) {
-  // candidates of the intermediate levels: two ping-pong buffers of (key, index) pairs
-  if (n_cap <= kCapLarge || k <= 0) return 0;
-  const int64_t chunks = (n_cap + kCapLarge - 1) / kCapLarge;
+  // candidates of the intermediate levels: two ping-pong buffers of (key, index) pairs, each large
+  // enough for the first level's output
+  if (n_cap <= kCapSmall || k <= 0) return 0;
+  const int64_t chunks = (n_cap + kCapSmall - 1) / kCapSmall;
   return 2 * (size_t)rows * chunks * k * 8;
 }
 
@@ -343,36 +346,38 @@ cudaError_t launch_topk(int B, const TopkParams& p, cudaStream_t st, bool pdl) {
   SelParams s;
   s.scores = p.scores; s.in_key = nullptr; s.in_idx = nullptr; s.n_in = p.n_cap; s.pos = p.pos;
   s.S = p.S; s.ratio = p.ratio; s.k = p.k;
-  if (p.n_cap <= kCapSmall && p.S > 1) {
-    s.chunk = (int)p.n_cap; s.n_chunks = 1; s.topk = p.topk; s.out_key = nullptr; s.out_idx = nullptr;
-    return launch_select<256>(s, rows, kCapSmall, st, pdl);
-  }
-  // level 0 over chunks of the scores, then levels over candidates until one CTA holds a row
   uint8_t* ws = static_cast<uint8_t*>(p.ws);
+  const size_t half = topk_workspace_bytes(rows, p.n_cap, p.k) / 2;
   int64_t n_in = p.n_cap;
-  int level = 0;
-  for (;;) {
-    const int64_t chunks = (n_in + kCapLarge - 1) / kCapLarge;
-    s.chunk = chunks == 1 ? (int)((n_in + 3) & ~3ll) : kCapLarge;
-    s.n_chunks = (int)chunks;
-    if (chunks == 1) {
+  for (int level = 0;; ++level) {
+    const bool first_launch = level == 0;
+    const bool dep = pdl || !first_launch;
+    if (n_in <= kCapSmall) {                                   // one small CTA holds the row: final level
+      s.chunk = (int)((n_in + 3) & ~3ll); s.n_chunks = 1;
       s.topk = p.topk; s.out_key = nullptr; s.out_idx = nullptr;
-      return launch_select<1024>(s, rows, kCapLarge, st, pdl || level > 0);
+      if (p.S > 1) return launch_select<256>(s, rows, kCapSmall, st, dep);
+      return launch_select<512>(s, rows, kCapSmall, st, dep);
+    }
+    if (level > 0 && n_in <= kCapLarge) {                      // one large CTA holds the row: final level
+      s.chunk = (int)((n_in + 3) & ~3ll); s.n_chunks = 1;
+      s.topk = p.topk; s.out_key = nullptr; s.out_idx = nullptr;
+      return launch_select<1024>(s, rows, kCapLarge, st, dep);
     }
     if (!ws) return cudaErrorInvalidValue;
-    // ping-pong halves of the candidate workspace
-    const size_t half = topk_workspace_bytes(rows, p.n_cap, p.k) / 2;
-    uint8_t* buf = ws + (level & 1) * half;
+    const int64_t cap = level == 0 ? kCapSmall : kCapLarge;
+    const int64_t chunks = (n_in + cap - 1) / cap;
     const int64_t n_out = chunks * p.k;
+    uint8_t* buf = ws + (level & 1) * half;
+    s.chunk = (int)cap; s.n_chunks = (int)chunks;
     s.topk = nullptr;
     s.out_key = reinterpret_cast<uint32_t*>(buf);
     s.out_idx = reinterpret_cast<int32_t*>(buf + (size_t)rows * n_out * 4);
-    cudaError_t e = launch_select<1024>(s, rows, kCapLarge, st, pdl || level > 0);
+    cudaError_t e = level == 0 ? launch_select<512>(s, rows, kCapSmall, st, dep)
+                               : launch_select<1024>(s, rows, kCapLarge, st, dep);
     if (e != cudaSuccess) return e;
     s.scores = nullptr; s.pos = nullptr;
     s.in_key = s.out_key; s.in_idx = s.out_idx; s.n_in = n_out;
     n_in = n_out;
-    ++level;
   }
 }
 
