@@ -129,6 +129,27 @@ cudaError_t launch_kernel(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 bl
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// Asks L2 to fetch `bytes` (a multiple of 16, 16-byte aligned) starting at p; nothing waits for it.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// ------------------------------------------------------------------ phase stamps
+// CSA_STAMP(slot) records %globaltimer for (CTA, slot) in a device table when the library is
+// compiled with -DCSA_TRACE (a timing build that also defines g_trace); otherwise it is nothing.
+#ifdef CSA_TRACE
+extern __device__ unsigned long long g_trace[8192][64];
+#define CSA_STAMP(slot)                                                                            \
+  do {                                                                                             \
+    unsigned long long t_;                                                                         \
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                                         \
+    const int c_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);                 \
+    if (c_ < 8192 && (slot) < 64) ::csa::g_trace[c_][(slot)] = t_;                                 \
+  } while (0)
+#else
+#define CSA_STAMP(slot) ((void)0)
+#endif
+
 // visible compressed entries of a query at t
 __device__ __forceinline__ int64_t visible_entries(int64_t t, int ratio) { return (t + 1) / ratio; }
 

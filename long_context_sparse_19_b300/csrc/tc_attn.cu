@@ -9,16 +9,23 @@
 // The same shared-memory KV data is the K-major A operand of the first product and, read along
 // the other axis, the MN-major A operand of the second.
 //
-// One CTA = one query and up to two 128-candidate tiles (window tiles first, then compressed
-// tiles), so that a decode step of 32 requests x 5 tiles fits one wave of CTAs. A tile streams
-// through a 4-stage ring in 32 KB K-chunks (128 candidates x 128 dims): the last tile of the
-// S^T phase stays resident for the O^T phase and only the other tile is gathered again (an L2
-// hit). Rows are gathered by warps 2..5 with 16-byte cp.async straight into the 128-byte
-// swizzled tensor-core layout; empty slots are zero-filled; raw window rows are rotated at their
-// own positions (RoPE on dims 448..511) in shared memory. Warp 0 loads Q by TMA and issues every
-// tcgen05.mma; warps 2..5 (thread = candidate row = TMEM lane) run the softmax on S^T read from
-// TMEM: per-head max and sum by a butterfly reduce-scatter across lanes plus a 4-warp combine,
-// P^T (bf16) into shared memory. They finally write the split partial (max, sum, O) in fp32.
+// One CTA = one query and one or two 128-candidate tiles (window tiles first, then compressed
+// tiles). Decode batches use one tile per CTA: the grid lists every query's window tile first and
+// those CTAs never wait for the selection kernel, so under programmatic dependent launch they run
+// while the selection is still being computed; the compressed tiles follow in one wave, their
+// rows already requested into L2 by the selection kernel. A tile streams through a 4-stage ring in
+// 32 KB K-chunks (128 candidates x 128 dims); with two tiles per CTA the last tile of the S^T phase
+// stays resident for the O^T phase and only the other one is gathered again (an L2 hit).
+// Warps:
+//   0    loads Q by TMA and issues every tcgen05.mma (one thread);
+//   1..5 gather the candidate rows with 16-byte cp.async straight into the 128-byte swizzled layout
+//        (random 1 KB rows: an SM sustains only tens of GB/s of such gathers, so many threads issue
+//        them and several chunks stay in flight); empty slots are zero-filled. Warp 1 also owns
+//        TMEM. Warps 2..5 (thread = candidate row = TMEM lane) then run the softmax on S^T read from
+//        TMEM: per-head max and sum by a butterfly reduce-scatter across lanes plus a 4-warp
+//        combine, P^T (bf16) into shared memory, and finally write the split partial (max, sum, O);
+//   6    rotates the query at t (RoPE on dims 448..511) in shared memory. Raw window rows are
+//        rotated at their own positions by the gather threads, each in the pieces it copied.
 #include <cudaTypedefs.h>
 
 #include "tc.h"
@@ -33,8 +40,8 @@ constexpr int kD = 512;
 constexpr int kH = 64;
 constexpr int kTile = 128;
 constexpr int kMaxTiles = 2;                        // tiles per CTA
-constexpr int kThreads = 192;
-constexpr int kStages = 4;
+constexpr int kThreads = 224;
+constexpr int kStages = 4;                          // = chunks per tile: chunk c always uses stage c
 constexpr uint32_t kBlk = kTile * 128;              // 16 KB: [128 rows][64 dims] swizzled
 constexpr uint32_t kChunkBytes = 2 * kBlk;          // 32 KB: 128 rows x 128 dims
 constexpr uint32_t kQBlock = kH * 128;              // 8 KB: [64 heads][64 dims]
@@ -44,12 +51,13 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = kMaxTiles * kH;          // O^T[dc] at kColO + 64 dc
 constexpr uint32_t kIdescS = idesc_bf16(128, 64, false, false);
 constexpr uint32_t kIdescO = idesc_bf16(128, 64, true, true);
+constexpr int kGatherThreads = 160;                 // warps 1..5
 constexpr size_t kAuxBytes = 2048;                   // barriers, row table, RoPE table (< 1.5 KB)
 constexpr size_t kSmemBytes = 1024 + kQBytes + kStages * kChunkBytes + kMaxTiles * kPBytes + kAuxBytes;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttnTcParams {
-  const __nv_bfloat16* kv;   // [B, N, 512] raw rows
+  const __nv_bfloat16* kv;   // [B, N, 512] raw rows (for L2 prefetch; loads go through the tensor maps)
   const __nv_bfloat16* ckv;  // [B, n_cap, 512]
   const int32_t* topk;       // [B, S, k] or null (HCA)
   const int64_t* pos;        // [B, S] or null (t = s)
@@ -62,6 +70,17 @@ struct AttnTcParams {
   int32_t* err;
 };
 
+// The loads of one CTA, in order: S^T phase i = 0 .. 4 nt - 1 (tile slot i / 4, chunk i % 4, fill
+// i / 4 of stage i % 4), then, for two tiles, the re-gather of tile slot 0 (fill 2 of stages 0..3).
+struct LoadSeq {
+  int nt;
+  __device__ int count() const { return 4 * nt + (nt > 1 ? 4 : 0); }
+  __device__ void at(int i, int& j, int& c, int& fill) const {
+    if (i < 4 * nt) { j = i >> 2; c = i & 3; fill = i >> 2; }
+    else { j = 0; c = i - 4 * nt; fill = 2; }
+  }
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const AttnTcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -70,10 +89,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ring = qs + kQBytes;                                // kStages x [2 blocks][128 rows][128 B]
   uint8_t* ps = ring + kStages * kChunkBytes;                  // kMaxTiles x [128 rows][128 B]
   uint64_t* bars = reinterpret_cast<uint64_t*>(ps + kMaxTiles * kPBytes);
-  uint64_t* full = bars;                                       // [kStages] (128 arrivals)
+  uint64_t* full = bars;                                       // [kStages] (kGatherThreads arrivals)
   uint64_t* empty = bars + kStages;                            // [kStages] (MMA commit)
   uint64_t* bar_q = bars + 2 * kStages;                        // Q bytes landed (tx)
-  uint64_t* bar_qrot = bar_q + 1;                              // Q rotated (64 arrivals)
+  uint64_t* bar_qrot = bar_q + 1;                              // Q rotated (32 arrivals)
   uint64_t* bar_s = bar_q + 2;                                 // S^T complete
   uint64_t* bar_p = bar_q + 3;                                 // P^T written (128 arrivals)
   uint64_t* bar_o = bar_q + 4;                                 // O^T complete
@@ -82,14 +101,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* th_hi = reinterpret_cast<float*>(rows_s + kMaxTiles * kTile);   // [32]
   float* th_lo = th_hi + 32;                                   // [32]
   int* tile_id = reinterpret_cast<int*>(th_lo + 32);           // [kMaxTiles]
+  float* q_cs = reinterpret_cast<float*>(tile_id + 4);         // [32] cos / sin of the query's angles
+  float* q_sn = q_cs + 32;                                     // [32]
   // softmax scratch lives in the Q buffer, which is dead once S^T is complete
   float* red = reinterpret_cast<float*>(qs);                   // [4][64]
   float* m_s = red + 4 * kH;                                   // [64]
 
+  if (threadIdx.x == 0) CSA_STAMP(0);
   griddep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z, s = blockIdx.y, cta = blockIdx.x;
-  const int64_t row = (int64_t)b * p.S + s;
+  // grid (rows, splits): every query's first tile (its window) is scheduled before any second tile
+  const int64_t row = blockIdx.x;
+  const int b = (int)(row / p.S), s = (int)(row % p.S), cta = blockIdx.y;
   const int64_t t = p.pos ? p.pos[row] : s;
   if (t < 0 || t >= p.N) {                                     // uniform over the CTA
     if (threadIdx.x == 0) set_error(p.err, DEVERR_BAD_POS);
@@ -102,20 +125,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_tiles = p.win_tiles + comp_tiles;
   const int first_tile = cta * p.tiles_per_cta;
   const int nt = min(p.tiles_per_cta, total_tiles - first_tile);   // >= 1 by construction of the grid
+  const LoadSeq seq{nt};
   // Processing order of the S^T phase: a window tile last, so that it is the resident tile of the
-  // O^T phase and never has to be rotated twice.
+  // O^T phase and is rotated only once.
   if (threadIdx.x < kMaxTiles) {
     int id = first_tile + (int)threadIdx.x;
     if (nt == 2 && first_tile < p.win_tiles) id = first_tile + 1 - (int)threadIdx.x;
     tile_id[threadIdx.x] = threadIdx.x < nt ? id : -1;
   }
-  __syncthreads();
-
   if (threadIdx.x < 32) { th_hi[threadIdx.x] = p.rope.th_hi[threadIdx.x]; th_lo[threadIdx.x] = p.rope.th_lo[threadIdx.x]; }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], 128); mbar_init(&empty[i], 1); }
+    for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], kGatherThreads); mbar_init(&empty[i], 1); }
     mbar_init(bar_q, 1);
-    mbar_init(bar_qrot, 64);
+    mbar_init(bar_qrot, 32);
     mbar_init(bar_s, 1);
     mbar_init(bar_p, 128);
     mbar_init(bar_o, 1);
@@ -125,12 +147,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (threadIdx.x == 0) {                                      // Q is an input of the call: load it now
+  if (threadIdx.x == 32) {                                     // Q is an input of the call: load it now
     prefetch_tensormap(&qmap);
     mbar_arrive_expect_tx(bar_q, kQBytes);
     for (int kb = 0; kb < 8; ++kb) tma_load_2d(qs + kb * kQBlock, &qmap, bar_q, kb * 64, (int32_t)(row * kH));
   }
-  griddep_wait();                                              // the selection comes from the previous kernel
+  // Only compressed tiles read the selection written by the previous kernel; window tiles read
+  // nothing it writes and proceed at once.
+  bool any_comp = false;
+  for (int j = 0; j < nt; ++j) any_comp |= tile_id[j] >= p.win_tiles;
+  if (any_comp) griddep_wait();
 
   // ---------------------------------------------------------------- candidate rows of the tiles
   for (int i = threadIdx.x; i < kMaxTiles * kTile; i += kThreads) {
@@ -154,24 +180,96 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     rows_s[i] = (int32_t)g;
+    // the gathers below are limited by how many requests one SM keeps in flight: have L2 fetch
+    // every row of the CTA at once (a no-op when the selection kernel already asked for it)
+    if (g >= 0) prefetch_l2((tid_ < p.win_tiles ? p.kv : p.ckv) + g * kD, kD * 2);
   }
   __syncthreads();
+  if (threadIdx.x == 0) CSA_STAMP(1);
   const uint32_t tmem = *tmem_slot;
-  // loads: S^T phase = nt tiles x 4 chunks (fills 0, 1); O^T phase re-gathers tile 0 when nt == 2 (fill 2)
-  const int n_loads_s = 4 * nt;
+  auto is_win = [&](int j) { return tile_id[j] < p.win_tiles; };
+  // ---------------------------------------------------------------- the gather (warps 1..5)
+  // Load i brings chunk c (dims 128c..128c+127) of the 128 rows of tile slot j into stage c: 2048
+  // pieces of 16 bytes, consecutive threads on consecutive pieces of a row. Empty slots are zeros.
+  const int gt = threadIdx.x - 32;                             // gather thread 0..159 (warps 1..5)
+  auto gather_issue = [&](int j, int c) {
+    uint8_t* stage = ring + c * kChunkBytes;
+    const __nv_bfloat16* base = is_win(j) ? p.kv : p.ckv;
+    for (int u = gt; u < 2048; u += kGatherThreads) {
+      const int rr = u >> 4, piece = u & 15;
+      uint8_t* dst = stage + (piece >> 3) * kBlk + sw128_offset(rr, piece & 7);
+      const int32_t g = rows_s[j * kTile + rr];
+      if (g >= 0) cp_async16(dst, base + (int64_t)g * kD + c * 128 + piece * 8);
+      else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    cp_async_commit();
+  };
+  // this thread's copies of load i landed: a raw window tile's chunk 3 holds the rotary dims
+  // 448..511 (block 1), which each thread rotates in the pieces it copied itself, at the row's own
+  // position; then the chunk is published to the tensor core
+  auto gather_complete = [&](int i) {
+    int j, c, fill;
+    seq.at(i, j, c, fill);
+    if (c == 3 && is_win(j)) {
+      uint8_t* blk1 = ring + 3 * kChunkBytes + kBlk;
+      for (int u = gt; u < 2048; u += kGatherThreads) {
+        const int rr = u >> 4, piece = u & 15;
+        if (piece < 8 || rows_s[j * kTile + rr] < 0) continue;
+        uint4* q16 = reinterpret_cast<uint4*>(blk1 + sw128_offset(rr, piece - 8));
+        uint4 v = *q16;
+        uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+        const int64_t pos = lo + (int64_t)tile_id[j] * kTile + rr;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int pair = (piece - 8) * 4 + k;
+          float cs, sn;
+          rope_cs(pos, th_hi[pair], th_lo[pair], cs, sn);
+          const float a = bf16lo(w[k]), bb = bf16hi(w[k]);
+          w[k] = pack_bf16(a * cs - bb * sn, a * sn + bb * cs);
+        }
+        *q16 = v;
+      }
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(&full[c]);
+  };
+  // loads [i0, i1) in order, up to kStages - 1 in flight per thread
+  auto gather_loads = [&](int i0, int i1, bool& ok) {
+    for (int i = i0; i < i1; ++i) {
+      int j, c, fill;
+      seq.at(i, j, c, fill);
+      if (fill > 0 && ok) ok = mbar_wait(&empty[c], (fill - 1) & 1, p.err);
+      if (ok) gather_issue(j, c);
+      else cp_async_commit();
+      if (gt == 0) CSA_STAMP(16 + i);
+      if (i - i0 >= kStages - 1) {
+        cp_async_wait<kStages - 1>();
+        gather_complete(i - (kStages - 1));
+      }
+    }
+    cp_async_wait<0>();
+    for (int i = i1 - (kStages - 1) > i0 ? i1 - (kStages - 1) : i0; i < i1; ++i) gather_complete(i);
+  };
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------------------------------------------------------- the MMA issuer
+      // ---------------------------------------------------------------- MMA issuer
       bool ok = mbar_wait(bar_q, 0, p.err) && mbar_wait(bar_qrot, 0, p.err);
+      CSA_STAMP(8);
       const uint32_t q_addr = smem_u32(qs), ring_addr = smem_u32(ring), p_addr = smem_u32(ps);
+      auto wait_load = [&](int i) {                            // load i landed (and was rotated if needed)
+        int j, c, fill;
+        seq.at(i, j, c, fill);
+        return mbar_wait(&full[c], fill & 1, p.err);
+      };
       // S^T phase
-      for (int q = 0; q < n_loads_s && ok; ++q) {
-        const int st = q % kStages, fill = q / kStages, j = q / 4, c = q % 4;
-        ok = mbar_wait(&full[st], fill & 1, p.err);
+      for (int q = 0; q < 4 * nt && ok; ++q) {
+        const int j = q >> 2, c = q & 3;
+        ok = wait_load(q);
         if (!ok) break;
+        CSA_STAMP(32 + q);
         tc_fence_after();
-        const uint32_t a0 = ring_addr + st * kChunkBytes;
+        const uint32_t a0 = ring_addr + c * kChunkBytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kBlk + (kk & 3) * 32;
@@ -179,91 +277,68 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16(tmem + j * kH, desc_kmajor_sw128(a0 + off), desc_kmajor_sw128(q_addr + qoff), kIdescS,
                    (c > 0 || kk > 0) ? 1u : 0u);
         }
-        if (j < nt - 1) mma_commit(&empty[st]);                // the last tile stays resident
+        if (j < nt - 1) mma_commit(&empty[c]);                 // the last tile stays resident
       }
       if (ok) mma_commit(bar_s);
+      CSA_STAMP(9);
       if (ok) ok = mbar_wait(bar_p, 0, p.err);
-      // O^T phase: the resident tile (tile nt-1, fill (nt-1) of stages 0..3), then tile 0 again
+      CSA_STAMP(10);
+      // O^T phase: the resident tile (slot nt-1), then slot 0 again
       for (int jj = 0; jj < nt && ok; ++jj) {
         const int j = nt - 1 - jj;
         for (int c = 0; c < 4 && ok; ++c) {
-          const int st = c;
-          if (jj > 0) {                                        // re-gathered chunk: fill 2
-            ok = mbar_wait(&full[st], 0, p.err);
+          if (jj > 0) {
+            ok = wait_load(4 * nt + c);
             if (!ok) break;
           }
           tc_fence_after();
-          const uint32_t a0 = ring_addr + st * kChunkBytes;
+          const uint32_t a0 = ring_addr + c * kChunkBytes;
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks) {
             mma_bf16(tmem + kColO + c * kH, desc_mnmajor_sw128(a0 + ks * 2048, kBlk),
                      desc_mnmajor_sw128(p_addr + j * kPBytes + ks * 2048, kBlk), kIdescO,
                      (jj > 0 || ks > 0) ? 1u : 0u);
           }
-          if (jj == 0 && nt > 1) mma_commit(&empty[st]);       // frees the stage for the re-gather
+          if (jj == 0 && nt > 1) mma_commit(&empty[c]);        // frees the stage for the re-gather
         }
       }
       if (ok) mma_commit(bar_o);
+      CSA_STAMP(11);
     }
-  } else if (warp >= 2) {
-    // ---------------------------------------------------------------- gather / softmax / epilogue warps
-    const int pt = threadIdx.x - 64;                           // 0..127
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- gather (warp 1 only gathers)
+    // Drain the S^T phase before the re-gather: its loads wait for the O^T MMAs, which need the
+    // softmax, which needs every S^T phase load completed by all gather threads.
+    bool ok = true;
+    gather_loads(0, 4 * nt, ok);
+    gather_loads(4 * nt, seq.count(), ok);
+  } else if (warp == 6) {
+    // ---------------------------------------------------------------- RoPE of the query
+    // every head is rotated at t: lane i computes pair i's cos / sin once, shared through registers
+    float cs_i, sn_i;
+    rope_cs(t, th_hi[lane], th_lo[lane], cs_i, sn_i);
+    q_cs[lane] = cs_i;
+    q_sn[lane] = sn_i;
+    __syncwarp();
+    bool ok = mbar_wait_warp(bar_q, 0, p.err);
+    if (ok) {
+      rope_line_tab(qs + 7 * kQBlock + lane * 128, lane, q_cs, q_sn);
+      rope_line_tab(qs + 7 * kQBlock + (lane + 32) * 128, lane + 32, q_cs, q_sn);
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(bar_qrot);
+    if (lane == 0) CSA_STAMP(2);
+  } else {
+    // ---------------------------------------------------------------- softmax / epilogue warps (2..5)
+    const int et = threadIdx.x - 64;                           // 0..127
     const int wq = warp & 3;                                   // TMEM lane quadrant
     const int r = 32 * wq + lane;                              // candidate row = TMEM lane
-    bool ok = true;
-    // Q rotation at t: thread h < 64 rotates head h's dims 448..511 once the TMA bytes landed
-    if (pt < kH) {
-      ok = mbar_wait(bar_q, 0, p.err);
-      if (ok) rope_line(qs + 7 * kQBlock + pt * 128, pt, t, th_hi, th_lo);
-      fence_proxy_async_smem();
-      mbar_arrive(bar_qrot);
-    }
-    // one load = 128 rows x 256 B of chunk c of tile slot j into ring stage st
-    auto issue = [&](int j, int c, int st) {
-      uint8_t* stage = ring + st * kChunkBytes;
-#pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const int u = pt + 128 * i;                            // (row, piece) pairs, 2 rows per warp
-        const int rr = u >> 4, piece = u & 15;
-        uint8_t* dst = stage + (piece >> 3) * kBlk + sw128_offset(rr, piece & 7);
-        const int32_t g = rows_s[j * kTile + rr];
-        const __nv_bfloat16* base = tile_id[j] < p.win_tiles ? p.kv : p.ckv;
-        if (g >= 0) cp_async16(dst, base + (int64_t)g * kD + c * 128 + piece * 8);
-        else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-      }
-      cp_async_commit();
-    };
-    // completes load (j, c) in stage st: rotate window rows (chunk 3), publish to the async proxy
-    auto finish = [&](int j, int c, int st) {
-      if (c == 3 && tile_id[j] < p.win_tiles) {
-        named_barrier(1, 128);                                 // every thread's copies of the chunk landed
-        const int32_t g = rows_s[j * kTile + pt];
-        if (g >= 0) rope_line(ring + st * kChunkBytes + kBlk + pt * 128, pt, lo + (int64_t)tile_id[j] * kTile + pt,
-                              th_hi, th_lo);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&full[st]);
-    };
-    // S^T phase loads: q -> (tile q/4, chunk q%4), stage q%4, fill q/4; up to kStages - 1 loads stay
-    // in flight while the oldest one is completed
-    for (int q = 0; q < n_loads_s; ++q) {
-      const int st = q % kStages, fill = q / kStages;
-      if (fill > 0 && ok) ok = mbar_wait(&empty[st], (fill - 1) & 1, p.err);
-      if (ok) issue(q / 4, q % 4, st);
-      else cp_async_commit();
-      if (q >= kStages - 1) {
-        cp_async_wait<kStages - 1>();
-        const int d = q - (kStages - 1);
-        finish(d / 4, d % 4, d % kStages);
-      }
-    }
-    cp_async_wait<0>();
-    for (int d = n_loads_s - (kStages - 1) > 0 ? n_loads_s - (kStages - 1) : 0; d < n_loads_s; ++d)
-      finish(d / 4, d % 4, d % kStages);
-
-    // ---------------------------------------------------------------- softmax over the CTA's candidates
+    const int wi = warp - 2;
+    bool gok = true;
+    gather_loads(0, 4 * nt, gok);                              // the S^T phase loads
     // TMEM loads are warp-collective: every lane loads, empty rows are masked afterwards
-    ok = mbar_wait_warp(bar_s, 0, p.err) && __all_sync(0xffffffffu, ok);
+    bool ok = mbar_wait_warp(bar_s, 0, p.err) && __all_sync(0xffffffffu, gok);
+    if (et == 0) CSA_STAMP(4);
     tc_fence_after();
     const uint32_t lane_base = tmem + ((wq * 32) << 16);
     float v[64];
@@ -279,18 +354,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < 32; ++h) v[half * 32 + h] = fmaxf(v[half * 32 + h], valid ? sv[h] : -INFINITY);
       }
     }
-    const int wi = warp - 2;
     reduce_scatter64<true>(v, lane);
     red[wi * kH + 2 * lane] = v[0];
     red[wi * kH + 2 * lane + 1] = v[1];
     named_barrier(1, 128);
-    if (pt < kH) m_s[pt] = fmaxf(fmaxf(red[pt], red[kH + pt]), fmaxf(red[2 * kH + pt], red[3 * kH + pt]));
+    if (et < kH) m_s[et] = fmaxf(fmaxf(red[et], red[kH + et]), fmaxf(red[2 * kH + et], red[3 * kH + et]));
     named_barrier(1, 128);
     const float c2 = p.scale * kLog2e;
 #pragma unroll
     for (int h = 0; h < 64; ++h) v[h] = 0.f;
-    for (int j = 0; j < kMaxTiles; ++j) {
-      if (j >= nt) break;
+    for (int j = 0; j < nt; ++j) {
       const bool valid = ok && rows_s[j * kTile + r] >= 0;
       uint8_t* line = ps + j * kPBytes;
 #pragma unroll
@@ -318,30 +391,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     fence_proxy_async_smem();
     mbar_arrive(bar_p);
-    // O^T phase: re-gather tile 0 of a two-tile CTA into stages 0..3 (fill 2)
-    if (nt > 1) {
-      for (int c = 0; c < 4; ++c) {
-        if (ok) ok = mbar_wait(&empty[c], 1, p.err);
-        if (ok) issue(0, c, c);
-        else cp_async_commit();
-      }
-      cp_async_wait<3>(); finish(0, 0, 0);
-      cp_async_wait<2>(); finish(0, 1, 1);
-      cp_async_wait<1>(); finish(0, 2, 2);
-      cp_async_wait<0>(); finish(0, 3, 3);
-    }
+    if (et == 0) CSA_STAMP(5);
+    gather_loads(4 * nt, seq.count(), gok);                    // two tiles: tile slot 0 again
     reduce_scatter64<false>(v, lane);
     red[wi * kH + 2 * lane] = v[0];
     red[wi * kH + 2 * lane + 1] = v[1];
     named_barrier(1, 128);
     const int64_t pi = (row * p.n_split + cta) * kH;
-    if (pt < kH) {
-      const float l = (red[pt] + red[kH + pt]) + (red[2 * kH + pt] + red[3 * kH + pt]);
-      p.part_ml[2 * (pi + pt)] = m_s[pt] == -INFINITY ? -INFINITY : m_s[pt] * p.scale;
-      p.part_ml[2 * (pi + pt) + 1] = l;
+    if (et < kH) {
+      const float l = (red[et] + red[kH + et]) + (red[2 * kH + et] + red[3 * kH + et]);
+      p.part_ml[2 * (pi + et)] = m_s[et] == -INFINITY ? -INFINITY : m_s[et] * p.scale;
+      p.part_ml[2 * (pi + et) + 1] = l;
     }
     // split partial O: thread = dim 128 dc + r, 64 heads
-    ok = mbar_wait_warp(bar_o, 0, p.err) && __all_sync(0xffffffffu, ok);
+    ok = mbar_wait_warp(bar_o, 0, p.err) && ok;
+    if (et == 0) CSA_STAMP(6);
     if (ok) {
       tc_fence_after();
 #pragma unroll 1
@@ -359,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) CSA_STAMP(12);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -378,9 +443,10 @@ static int attn_tiles(int window, int top_k, int64_t n_cap) {
   return wt + (int)ct;
 }
 
-// Tiles per CTA: one when every tile of the batch fits one wave of CTAs, otherwise two.
+// Tiles per CTA: one (no tile is ever gathered twice) while the batch's tiles fit two waves of
+// CTAs - the first wave is mostly window tiles, which run during the selection kernel - else two.
 static int attn_tiles_per_cta(int rows, int tiles) {
-  return (int64_t)rows * tiles <= tc_sm_count() ? 1 : 2;
+  return (int64_t)rows * tiles <= 2 * (int64_t)tc_sm_count() ? 1 : 2;
 }
 
 int tc_attn_splits(int window, int top_k, int64_t n_cap, int rows) {
@@ -411,7 +477,7 @@ cudaError_t tc_sparse_attn(int B, const AttnParams& a, void*, cudaStream_t st, b
   p.S = a.S; p.k = a.k; p.ratio = a.ratio; p.window = a.window; p.n_split = a.n_split;
   p.win_tiles = (a.window + kTile - 1) / kTile; p.tiles_per_cta = per;
   p.scale = a.scale; p.rope = a.rope; p.err = a.err;
-  dim3 grid((unsigned)a.n_split, (unsigned)a.S, (unsigned)B);
+  dim3 grid((unsigned)rows, (unsigned)a.n_split);
   return launch_kernel(pdl, attn_tc_kernel, grid, dim3(kThreads), kSmemBytes, st, qmap, p);
 }
 

@@ -15,8 +15,8 @@
 //            half normalised and written as the final output (inverse RoPE on dims 448..511).
 // The KV data streams through a 4-stage ring of 32 KB K-chunks twice (phase S, then phase O; the
 // second pass hits L2). Warps: 0 = Q TMA + tcgen05.mma issuer, 1 = TMEM owner + Q rotation,
-// 2..5 = softmax / epilogue (thread = TMEM lane), 6..7 = cp.async gather producers (raw window rows
-// are rotated at their own positions in shared memory).
+// 2..5 = softmax / epilogue (thread = TMEM lane), 6 = TMA gather producer (tile::gather4, lane g
+// handles rows 4g..4g+3), 7 = RoPE of the raw window rows at their own positions in shared memory.
 #include <cudaTypedefs.h>
 
 #include "tc.h"
@@ -32,7 +32,6 @@ constexpr int kH = 64;
 constexpr int kTile = 128;
 constexpr int kMaxTiles = 5;
 constexpr int kThreads = 256;
-constexpr int kProducers = 64;                      // warps 6..7
 constexpr int kStages = 4;
 constexpr uint32_t kBlk = kTile * 128;              // 16 KB: [128 rows][64 dims] swizzled
 constexpr uint32_t kChunkBytes = 2 * kBlk;          // 32 KB: 128 rows x 128 dims
@@ -49,8 +48,6 @@ constexpr size_t kSmemBytes = 1024 + kQPBytes + kStages * kChunkBytes + kAuxByte
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct PrefillParams {
-  const __nv_bfloat16* kv;   // [B, N, 512]
-  const __nv_bfloat16* ckv;  // [B, n_cap, 512]
   const int32_t* topk;       // [B, S, k] or null (HCA)
   const int64_t* pos;        // [B, S] or null (t = s)
   const float* sink;         // [64]
@@ -63,14 +60,15 @@ struct PrefillParams {
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const PrefillParams p) {
+    attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kvmap,
+                        const __grid_constant__ CUtensorMap ckvmap, const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qs = smem;                                          // Q: [8 blocks][64 heads][128 B]
   uint8_t* ps = smem;                                          // P^T: [5 tiles][128 rows][128 B] (after phase S)
   uint8_t* ring = smem + kQPBytes;                             // kStages x [2 blocks][128 rows][128 B]
   uint64_t* bars = reinterpret_cast<uint64_t*>(ring + kStages * kChunkBytes);
-  uint64_t* full = bars;                                       // [kStages] (kProducers arrivals)
+  uint64_t* full = bars;                                       // [kStages] (1 arrival + tx bytes)
   uint64_t* empty = bars + kStages;                            // [kStages] (MMA commit)
   uint64_t* bar_q = bars + 2 * kStages;                        // Q landed (tx)
   uint64_t* bar_qrot = bar_q + 1;                              // Q rotated (32 arrivals)
@@ -79,6 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_o0 = bar_q + 4;                                // O^T half 0 complete
   uint64_t* bar_e0 = bar_q + 5;                                // O^T half 0 read (128 arrivals)
   uint64_t* bar_o1 = bar_q + 6;                                // O^T half 1 complete
+  uint64_t* full_win = bar_q + 7;                              // a window chunk 3 landed (tx)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_q + 8);
   int32_t* rows_s = reinterpret_cast<int32_t*>(bar_q + 10);    // [5][128] global row (-1 = empty)
   float* th_hi = reinterpret_cast<float*>(rows_s + kMaxTiles * kTile);   // [32]
@@ -86,6 +85,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* red = th_lo + 32;                                     // [4][64]
   float* mx_s = red + 4 * kH;                                  // [64] max of scale * s and the sink
   float* il_s = mx_s + kH;                                     // [64] 1 / denominator
+  float* q_cs = il_s + kH;                                     // [32] cos / sin of the query's angles
+  float* q_sn = q_cs + 32;                                     // [32]
 
   griddep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -103,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x < 32) { th_hi[threadIdx.x] = p.rope.th_hi[threadIdx.x]; th_lo[threadIdx.x] = p.rope.th_lo[threadIdx.x]; }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], kProducers); mbar_init(&empty[i], 1); }
+    for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
     mbar_init(bar_q, 1);
     mbar_init(bar_qrot, 32);
     mbar_init(bar_s, 1);
@@ -111,6 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_o0, 1);
     mbar_init(bar_e0, 128);
     mbar_init(bar_o1, 1);
+    mbar_init(full_win, 1);
     fence_mbar_init();
   }
   if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
@@ -119,6 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   if (threadIdx.x == 0) {
     prefetch_tensormap(&qmap);
+    prefetch_tensormap(&kvmap);
+    prefetch_tensormap(&ckvmap);
     mbar_arrive_expect_tx(bar_q, kQBytes);
     for (int kb = 0; kb < 8; ++kb) tma_load_2d(qs + kb * kQBlock, &qmap, bar_q, kb * 64, (int32_t)(row * kH));
   }
@@ -201,62 +205,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- Q rotation at t
-    bool ok = mbar_wait(bar_q, 0, p.err);
+    // every head is rotated at t: lane i computes pair i's cos / sin once, shared through registers
+    float cs_i, sn_i;
+    rope_cs(t, th_hi[lane], th_lo[lane], cs_i, sn_i);
+    q_cs[lane] = cs_i;
+    q_sn[lane] = sn_i;
+    __syncwarp();
+    bool ok = mbar_wait_warp(bar_q, 0, p.err);
     if (ok) {
-      rope_line(qs + 7 * kQBlock + lane * 128, lane, t, th_hi, th_lo);
-      rope_line(qs + 7 * kQBlock + (lane + 32) * 128, lane + 32, t, th_hi, th_lo);
+      rope_line_tab(qs + 7 * kQBlock + lane * 128, lane, q_cs, q_sn);
+      rope_line_tab(qs + 7 * kQBlock + (lane + 32) * 128, lane + 32, q_cs, q_sn);
     }
     fence_proxy_async_smem();
     mbar_arrive(bar_qrot);
-  } else if (warp >= 6) {
-    // ---------------------------------------------------------------- gather producers
-    const int pt = threadIdx.x - (kThreads - kProducers);     // 0..63
+  } else if (warp == 6) {
+    // ---------------------------------------------------------------- TMA gather producer
     bool ok = true;
-    auto issue = [&](int j, int c, int st) {
-      uint8_t* stage = ring + st * kChunkBytes;
-      const __nv_bfloat16* base = j < p.win_tiles ? p.kv : p.ckv;
-#pragma unroll 4
-      for (int i = 0; i < 32; ++i) {
-        const int u = pt + kProducers * i;                     // (row, piece): 16 pieces of 16 B per row
-        const int rr = u >> 4, piece = u & 15;
-        uint8_t* dst = stage + (piece >> 3) * kBlk + sw128_offset(rr, piece & 7);
-        const int32_t g = rows_s[j * kTile + rr];
-        if (g >= 0) cp_async16(dst, base + (int64_t)g * kD + c * 128 + piece * 8);
-        else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    for (int q = 0; q < 2 * n_loads; ++q) {
+      const int st = q % kStages, fill = q / kStages;
+      int j, c;
+      load_of(q, j, c);
+      if (fill > 0 && ok) ok = mbar_wait_warp(&empty[st], (fill - 1) & 1, p.err);
+      // lane = group of rows 4 lane .. 4 lane + 3; empty slots repeat a valid row of the group
+      int32_t r4[4];
+      int32_t first = -1;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        r4[u] = rows_s[j * kTile + 4 * lane + u];
+        if (first < 0 && r4[u] >= 0) first = r4[u];
       }
-      cp_async_commit();
-    };
-    auto finish = [&](int j, int c, int st) {
-      if (c == 3 && j < p.win_tiles) {                         // raw window rows: RoPE at their positions
-        named_barrier(2, kProducers);
-        for (int rr = pt; rr < kTile; rr += kProducers) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) r4[u] = r4[u] >= 0 ? r4[u] : first;
+      uint8_t* stage = ring + st * kChunkBytes;
+      const bool live = ok && first >= 0;
+      if (!live) {                                             // no valid row (or an abandoned load): zeros
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          uint4* z = reinterpret_cast<uint4*>(stage + blk * kBlk + lane * 512);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) z[e] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();
+      const unsigned issue = __ballot_sync(0xffffffffu, live);
+      uint64_t* bar = (c == 3 && j < p.win_tiles) ? full_win : &full[st];
+      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(issue) * 2u * 512u);
+      __syncwarp();
+      if (live) {
+        const CUtensorMap* map = j < p.win_tiles ? &kvmap : &ckvmap;
+        tma_gather4(stage + lane * 512, map, bar, c * 128, r4[0], r4[1], r4[2], r4[3]);
+        tma_gather4(stage + kBlk + lane * 512, map, bar, c * 128 + 64, r4[0], r4[1], r4[2], r4[3]);
+      }
+    }
+  } else if (warp == 7) {
+    // ---------------------------------------------------------------- RoPE of raw window rows
+    // A window tile's chunk 3 lands on full_win; once rotated, this warp completes the stage's
+    // own barrier, so the MMA only waits on full[stage], in order.
+    bool ok = true;
+    int n_win_loads = 0;
+    for (int q = 0; q < 2 * n_loads; ++q) {
+      int j, c;
+      load_of(q, j, c);
+      if (c != 3 || j >= p.win_tiles) continue;
+      const int st = q % kStages;
+      if (ok) ok = mbar_wait_warp(full_win, n_win_loads & 1, p.err);
+      ++n_win_loads;
+      if (ok) {
+        for (int rr = lane; rr < kTile; rr += 32) {
           if (rows_s[j * kTile + rr] >= 0)
             rope_line(ring + st * kChunkBytes + kBlk + rr * 128, rr, lo + (int64_t)j * kTile + rr, th_hi, th_lo);
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(&full[st]);
-    };
-    for (int q = 0; q < 2 * n_loads; ++q) {
-      const int st = q % kStages, fill = q / kStages;
-      int j, c;
-      load_of(q, j, c);
-      if (fill > 0 && ok) ok = mbar_wait(&empty[st], (fill - 1) & 1, p.err);
-      if (ok) issue(j, c, st);
-      else cp_async_commit();
-      if (q >= kStages - 1) {                                  // up to kStages - 1 loads in flight
-        const int d = q - (kStages - 1);
-        int jp, cp;
-        load_of(d, jp, cp);
-        cp_async_wait<kStages - 1>();
-        finish(jp, cp, d % kStages);
-      }
-    }
-    cp_async_wait<0>();
-    for (int d = 2 * n_loads - (kStages - 1) > 0 ? 2 * n_loads - (kStages - 1) : 0; d < 2 * n_loads; ++d) {
-      int jl, cl;
-      load_of(d, jl, cl);
-      finish(jl, cl, d % kStages);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[st]);
     }
   } else {
     // ---------------------------------------------------------------- softmax / epilogue (warps 2..5)
@@ -389,17 +411,17 @@ cudaError_t tc_attn_prefill(int B, const AttnParams& a, cudaStream_t st, bool pd
   const int64_t comp = a.k > 0 ? (a.k + kTile - 1) / kTile : (a.n_cap + kTile - 1) / kTile;
   if (win_tiles + comp > kMaxTiles) return cudaErrorInvalidValue;
   if ((int64_t)B * a.N >= (int64_t)1 << 31 || (int64_t)B * a.n_cap >= (int64_t)1 << 31) return cudaErrorInvalidValue;
-  CUtensorMap qmap;
+  CUtensorMap qmap, kvmap, ckvmap;
   cudaError_t e = make_tmap_2d(&qmap, a.q, (int64_t)B * a.S * kH, kD, kH);
+  if (e == cudaSuccess) e = make_tmap_2d(&kvmap, a.kv, (int64_t)B * a.N, kD, 1);
+  if (e == cudaSuccess) e = make_tmap_2d(&ckvmap, a.ckv, (int64_t)B * a.n_cap, kD, 1);
   if (e != cudaSuccess) return e;
   PrefillParams p;
-  p.kv = static_cast<const __nv_bfloat16*>(a.kv);
-  p.ckv = static_cast<const __nv_bfloat16*>(a.ckv);
   p.topk = a.topk; p.pos = a.pos; p.sink = a.sink; p.out = static_cast<__nv_bfloat16*>(a.out);
   p.N = a.N; p.n_cap = a.n_cap; p.S = a.S; p.k = a.k; p.ratio = a.ratio; p.window = a.window;
   p.win_tiles = win_tiles; p.n_tiles = win_tiles + (int)comp; p.scale = a.scale; p.rope = a.rope; p.err = a.err;
   dim3 grid((unsigned)a.S, (unsigned)B);
-  return launch_kernel(pdl, attn_prefill_kernel, grid, dim3(kThreads), kSmemBytes, st, qmap, p);
+  return launch_kernel(pdl, attn_prefill_kernel, grid, dim3(kThreads), kSmemBytes, st, qmap, kvmap, ckvmap, p);
 }
 
 }  // namespace csa

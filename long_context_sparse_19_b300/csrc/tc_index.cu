@@ -93,14 +93,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0) {
       prefetch_tensormap(&cmap);
       griddep_wait();                                       // the cache may come from the previous kernel
+      // the cache streams through once: keep it from evicting the scores the selection reads next
+      const uint64_t policy = l2_evict_first_policy();
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages;
         if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1, p.err)) break;
         mbar_arrive_expect_tx(&full[st], kTileBytes);
         const int32_t y = (int32_t)(b * p.n_cap + (tile0 + i) * kTileM);
         uint8_t* dst = stage_base + st * kTileBytes;
-        tma_load_2d(dst, &cmap, &full[st], 0, y);
-        tma_load_2d(dst + kBlockBytes, &cmap, &full[st], 64, y);
+        tma_load_2d_hint(dst, &cmap, &full[st], 0, y, policy);
+        tma_load_2d_hint(dst + kBlockBytes, &cmap, &full[st], 64, y, policy);
       }
     }
   } else if (warp == 1) {

@@ -35,6 +35,10 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
@@ -87,6 +91,33 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Gathers 4 rows (r0..r3) x one box width of a 2-D tensor (box height 1) into 4 consecutive box
+// rows at dst (the map's swizzle applies, by destination address); completes on `bar` (tx bytes).
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x, int32_t r0,
+                                            int32_t r1, int32_t r2, int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// L2 policy for data read once and not needed again (a streamed cache): evicted first
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
+                                                 int32_t y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 
@@ -196,6 +227,23 @@ __device__ __forceinline__ void rope_line(uint8_t* line_base, uint32_t row, int6
     for (int k = 0; k < 4; ++k) {
       float c, s;
       rope_cs(pos, th_hi[ch * 4 + k], th_lo[ch * 4 + k], c, s);
+      const float a = bf16lo(w[k]), b = bf16hi(w[k]);
+      w[k] = pack_bf16(a * c - b * s, a * s + b * c);
+    }
+    *p = u;
+  }
+}
+
+// rotate the 32 pairs of one 128-byte swizzled line by precomputed cos / sin of each pair
+__device__ __forceinline__ void rope_line_tab(uint8_t* line_base, uint32_t row, const float* cs, const float* sn) {
+#pragma unroll 2
+  for (int ch = 0; ch < 8; ++ch) {
+    uint4* p = reinterpret_cast<uint4*>(line_base + ((ch ^ (row & 7u)) << 4));
+    uint4 u = *p;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float c = cs[ch * 4 + k], s = sn[ch * 4 + k];
       const float a = bf16lo(w[k]), b = bf16hi(w[k]);
       w[k] = pack_bf16(a * c - b * s, a * s + b * c);
     }

@@ -6,21 +6,23 @@
 // taken first); when fewer than k entries are visible every visible entry is taken. The selected
 // entries are written in ascending entry index, followed by -1 in the unused slots.
 //
-// Method. Float scores map to order-preserving 32-bit keys. One CTA selects from at most `cap`
-// items, loaded into shared memory once:
-//   1. an 11-bit histogram of the keys (shared-memory atomics) locates the bin
-//      that holds the k-th largest key;
-//   2. the items of that bin are listed and an MSB radix select over their lower 21 bits finds
-//      the exact threshold key T and how many items equal to T are taken;
-//   3. one order-preserving compaction (warp ballots and scans, four items per lane) writes every
-//      item above T and the first needed items equal to T, in index order.
-// Rows longer than one CTA's capacity are cut into chunks; each chunk's winners (a superset of
-// the row's winners inside the chunk) become (key, index) candidates, still in index order, and
-// a further level selects among them until one CTA holds the whole row.
+// Method. Float scores map to order-preserving 32-bit keys (0 marks an empty item). One CTA holds
+// up to 16 items per thread in registers, thread t owning items 16t .. 16t+15, so index order is
+// thread order. An MSB radix select finds the threshold key T: digits of 11, 11 and 10 bits, each
+// a shared-memory histogram over the items still matching the prefix (the first, over all items,
+// in per-warp private histograms so that warps never contend), a block-wide scan of the bins, and
+// an early exit once the threshold digit's bin holds exactly the items still needed. One
+// order-preserving compaction (block scans of per-thread counts) then writes every item above T and
+// the first needed items equal to T. Long rows are cut into chunks; each chunk's winners (a
+// superset of the row's winners inside the chunk) become (key, index) candidates, still in index
+// order, and a further level selects among them.
 #include "kernels.h"
 
 namespace csa {
 namespace {
+
+constexpr int kItems = 16;                  // items per thread
+constexpr int kBins = 2048;                 // 11-bit digits
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -35,69 +37,99 @@ struct SelParams {
   int64_t n_in;              // items per row of the input (n_cap at level 0)
   const int64_t* pos;        // [rows] query positions (level 0 visibility); null: t = row % S
   int S, ratio, k;
-  int chunk;                 // items per CTA (blockIdx.x selects the chunk), a multiple of 4
+  int chunk;                 // items per CTA (blockIdx.x selects the chunk)
   int n_chunks;
   int32_t* topk;             // final level: [rows, k], ascending entry index, -1 padded
   uint32_t* out_key;         // otherwise: [rows, n_chunks * k] candidates (-1 padded)
   int32_t* out_idx;
+  // final level only, optional: L2 prefetch of the selected ckv rows, the window and the q rows
+  const uint8_t* pf_ckv;
+  const uint8_t* pf_kv;
+  const uint8_t* pf_q;
+  int64_t pf_n_cap, pf_N;
+  int pf_row_bytes, pf_window, pf_q_bytes;
 };
-
-constexpr int kBins = 2048;                 // first-level histogram: the top 11 key bits
-constexpr int kShift0 = 21;
 
 template <int kThreads>
 struct SelSmem {
-  static size_t bytes(int cap, bool with_idx) {
-    // keys, (indices), bin list, histogram, scan scratch
-    return (size_t)cap * 4 * (with_idx ? 3 : 2) + kBins * 4 + 4 * 64 * 4 + 64;
-  }
+  static constexpr int kWarps = kThreads / 32;
+  // per-warp histograms of the first digit: two 16-bit counters per word
+  static constexpr size_t kWarpHist = (size_t)kWarps * (kBins / 2) * 4;
+  static constexpr size_t kBytes = kWarpHist + kBins * 4 + 4 * 32 * 4 + 64;
 };
 
-// block-wide exclusive scan of one value per thread (kThreads <= 1024); returns the exclusive
-// prefix and writes the block total to *total. `scratch` holds 32 words.
+// block-wide exclusive scan of two counters per thread (kThreads <= 1024), thread order;
+// scratch holds 64 words. Returns the exclusive prefixes and the totals.
 template <int kThreads>
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratch, uint32_t* total) {
+__device__ __forceinline__ void block_scan2(uint32_t a, uint32_t b, uint32_t* scratch, uint32_t& ea,
+                                            uint32_t& eb, uint32_t& ta, uint32_t& tb) {
   constexpr int kWarps = kThreads / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t incl = v;
+  uint32_t ia = a, ib = b;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += x;
+    const uint32_t xa = __shfl_up_sync(0xffffffffu, ia, o);
+    const uint32_t xb = __shfl_up_sync(0xffffffffu, ib, o);
+    if (lane >= o) { ia += xa; ib += xb; }
   }
-  if (lane == 31) scratch[warp] = incl;
+  if (lane == 31) { scratch[warp] = ia; scratch[32 + warp] = ib; }
   __syncthreads();
-  uint32_t wo = 0, tot = 0;
+  uint32_t wa = 0, wb = 0, sa = 0, sb = 0;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) {
-    const uint32_t s = scratch[w];
-    wo += (w < warp) ? s : 0u;
-    tot += s;
+    const uint32_t va = scratch[w], vb = scratch[32 + w];
+    if (w < warp) { wa += va; wb += vb; }
+    sa += va; sb += vb;
   }
   __syncthreads();
-  *total = tot;
-  return wo + incl - v;
+  ea = wa + ia - a; eb = wb + ib - b; ta = sa; tb = sb;
+}
+
+// Finds the bin holding the need-th largest item: bins are scanned from the top; thread t owns
+// kBins / kThreads consecutive bins (descending). Writes the bin, the items still needed from it
+// and that bin's count to out[0..2] (then visible to the whole block).
+template <int kThreads>
+__device__ __forceinline__ void find_bin(const uint32_t* hist, uint32_t need, uint32_t* scratch, uint32_t* out) {
+  constexpr int kPer = kBins / kThreads;
+  uint32_t c[kPer], tot = 0;
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) { c[u] = hist[kBins - 1 - kPer * threadIdx.x - u]; tot += c[u]; }
+  uint32_t ex, dummy, all, dummy2;
+  block_scan2<kThreads>(tot, 0u, scratch, ex, dummy, all, dummy2);
+  if (ex < need && need <= ex + tot) {
+    uint32_t run = ex;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      if (run < need && need <= run + c[u]) {
+        out[0] = kBins - 1 - kPer * threadIdx.x - u;
+        out[1] = need - run;
+        out[2] = c[u];
+      }
+      run += c[u];
+    }
+  }
+  __syncthreads();
 }
 
 template <int kThreads>
-__global__ void __launch_bounds__(kThreads) topk_select_kernel(const SelParams p, int cap) {
+__global__ void __launch_bounds__(kThreads) topk_select_kernel(const SelParams p) {
   constexpr int kWarps = kThreads / 32;
   extern __shared__ __align__(16) uint8_t sm[];
-  const bool level0 = p.scores != nullptr;
-  uint32_t* keys = reinterpret_cast<uint32_t*>(sm);                              // [cap]
-  int32_t* idxs = reinterpret_cast<int32_t*>(keys + cap);                        // [cap] (levels > 0)
-  uint32_t* list = level0 ? reinterpret_cast<uint32_t*>(idxs) : reinterpret_cast<uint32_t*>(idxs + cap);  // [cap]
-  uint32_t* hist = list + cap;                                                   // [kBins]
-  uint32_t* scr = hist + kBins;                                                  // [4][64]
-  __shared__ uint32_t s_T, s_need, s_cls, s_nlist, s_nvalid, s_bin, s_need_bin;
+  uint32_t* whist = reinterpret_cast<uint32_t*>(sm);                // [kWarps][kBins / 2]
+  uint32_t* hist = whist + kWarps * (kBins / 2);                    // [kBins]
+  uint32_t* scr = hist + kBins;                                     // [128]
+  uint32_t* res = scr + 128;                                        // [16]
 
+  if (threadIdx.x == 0) CSA_STAMP(0);
   griddep_launch();
   griddep_wait();
+  if (threadIdx.x == 0) CSA_STAMP(1);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.y;
   const int64_t c0 = (int64_t)blockIdx.x * p.chunk;
+  const bool level0 = p.scores != nullptr;
 
-  // ---- load the items of this CTA: level 0 = visible entries of the chunk, else the candidates
+  // ---- the items of this CTA: level 0 = visible entries of the chunk, else the candidates
   int n;
   if (level0) {
     const int64_t t = p.pos ? p.pos[row] : (row % p.S);
@@ -106,238 +138,176 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const SelParams p
   } else {
     n = (int)max((int64_t)0, min((int64_t)p.chunk, p.n_in - c0));
   }
-  const int n4 = (n + 3) & ~3;
-  for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
-  if (tid == 0) { s_nlist = 0; s_nvalid = 0; }
+  uint32_t key[kItems];
+  int32_t id[kItems];
+  const int i0 = tid * kItems;
+  if (level0) {
+    const float* sc = p.scores + row * p.n_in + c0 + i0;
+    if (((row * p.n_in + c0) & 3) == 0 && i0 + kItems <= n) {       // 16-byte aligned, all in range
+#pragma unroll
+      for (int q = 0; q < kItems / 4; ++q) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(sc) + q);
+        key[4 * q] = order_key(f.x); key[4 * q + 1] = order_key(f.y);
+        key[4 * q + 2] = order_key(f.z); key[4 * q + 3] = order_key(f.w);
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kItems; ++u) key[u] = i0 + u < n ? order_key(__ldg(sc + u)) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) id[u] = (int32_t)(c0 + i0 + u);
+  } else {
+    const uint32_t* ik = p.in_key + row * p.n_in + c0 + i0;
+    const int32_t* ii = p.in_idx + row * p.n_in + c0 + i0;
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) id[u] = i0 + u < n ? __ldg(ii + u) : -1;
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) key[u] = id[u] >= 0 ? __ldg(ik + u) : 0u;
+  }
+
+  // ---- first digit (key bits 31..21): per-warp private histograms, then summed
+  if (tid == 0) CSA_STAMP(2);
+  {
+    uint4* z = reinterpret_cast<uint4*>(whist);
+    for (int i = tid; i < kWarps * (kBins / 2) / 4; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+    if (tid < 16) res[tid] = 0;
+  }
   __syncthreads();
   {
-    const bool vec = ((row * p.n_in + c0) & 3) == 0;      // 16-byte aligned score rows
+    uint32_t* wh = whist + warp * (kBins / 2);
     uint32_t nv = 0;
-    for (int i = 4 * tid; i < n4; i += 4 * kThreads) {
-      uint32_t kq[4];
-      int32_t iq[4] = {0, 0, 0, 0};
-      if (level0) {
-        const float* sc = p.scores + row * p.n_in + c0 + i;
-        if (vec && i + 4 <= n) {
-          const float4 f = __ldg(reinterpret_cast<const float4*>(sc));
-          kq[0] = order_key(f.x); kq[1] = order_key(f.y); kq[2] = order_key(f.z); kq[3] = order_key(f.w);
-        } else {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) kq[u] = (i + u < n) ? order_key(__ldg(sc + u)) : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) nv += (i + u < n);
-      } else {
-        const uint32_t* ik = p.in_key + row * p.n_in + c0 + i;
-        const int32_t* ii = p.in_idx + row * p.n_in + c0 + i;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          iq[u] = (i + u < n) ? __ldg(ii + u) : -1;
-          kq[u] = iq[u] >= 0 ? __ldg(ik + u) : 0u;
-          nv += iq[u] >= 0;
-        }
-        *reinterpret_cast<int4*>(idxs + i) = make_int4(iq[0], iq[1], iq[2], iq[3]);
-      }
-      *reinterpret_cast<uint4*>(keys + i) = make_uint4(kq[0], kq[1], kq[2], kq[3]);
-      // histogram of the top 11 bits (valid items have keys > 0)
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (kq[u] != 0u) atomicAdd(&hist[kq[u] >> kShift0], 1u);
+    for (int u = 0; u < kItems; ++u) {
+      if (key[u] != 0u) {
+        const uint32_t b = key[u] >> 21;
+        atomicAdd(&wh[b >> 1], 1u << ((b & 1u) * 16));
+        ++nv;
       }
     }
     nv = __reduce_add_sync(0xffffffffu, nv);
-    if (lane == 0 && nv) atomicAdd(&s_nvalid, nv);
+    if (lane == 0 && nv) atomicAdd(&res[8], nv);
   }
   __syncthreads();
-  const uint32_t n_valid = s_nvalid;
+  if (tid == 0) CSA_STAMP(3);
+  for (int b2 = tid; b2 < kBins / 2; b2 += kThreads) {
+    uint32_t lo = 0, hi = 0;
+#pragma unroll 4
+    for (int w = 0; w < kWarps; ++w) {
+      const uint32_t v = whist[w * (kBins / 2) + b2];
+      lo += v & 0xffffu;
+      hi += v >> 16;
+    }
+    hist[2 * b2] = lo;
+    hist[2 * b2 + 1] = hi;
+  }
+  __syncthreads();
+  if (tid == 0) CSA_STAMP(4);
+  const uint32_t n_valid = res[8];
   const uint32_t kk = min((uint32_t)p.k, n_valid);
   const bool take_all = kk >= n_valid;
 
-  // take keys with (key & pmask) > T, and the first need_t with (key & pmask) == T
-  uint32_t T = 0, need_t = 0, pmask = ~0u;
+  // ---- radix select of the threshold: taken = (key & pmask) > prefix, or == prefix for the first
+  // `need` such items in index order
+  uint32_t prefix = 0, pmask = 0, need = kk;
   if (!take_all) {
-    // ---- 1. the bin of the kk-th largest key: thread t scans bins in descending order
-    constexpr int kPer = kBins / kThreads;      // bins per thread
-    uint32_t c[kPer], tot = 0;
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) { c[u] = hist[kBins - 1 - kPer * tid - u]; tot += c[u]; }
-    uint32_t all;
-    const uint32_t excl = block_excl_scan<kThreads>(tot, scr, &all);
-    if (excl < kk && kk <= excl + tot) {
-      uint32_t run = excl;
-#pragma unroll
-      for (int u = 0; u < kPer; ++u) {
-        if (run < kk && kk <= run + c[u]) { s_bin = kBins - 1 - kPer * tid - u; s_need_bin = kk - run; }
-        run += c[u];
-      }
-    }
-    __syncthreads();
-    const uint32_t bin = s_bin;
-    uint32_t need = s_need_bin;                  // items still needed from the bin
-    // ---- 2. list the bin's keys, then radix-select the need-th largest among them
-    for (int i = tid; i < n; i += kThreads) {
-      const unsigned am = __activemask();
-      const uint32_t key = keys[i];
-      const bool in = key != 0u && (key >> kShift0) == bin;
-      const unsigned b = __ballot_sync(am, in);
-      if (b) {
-        const int leader = __ffs(b) - 1;
-        uint32_t base = 0;
-        if (lane == leader) base = atomicAdd(&s_nlist, (uint32_t)__popc(b));
-        base = __shfl_sync(am, base, leader);
-        if (in) list[base + __popc(b & ((1u << lane) - 1u))] = key;
-      }
-    }
-    __syncthreads();
-    const uint32_t nl = s_nlist;
-    uint32_t prefix = bin << kShift0;
-    pmask = ~0u << kShift0;
-    uint32_t cls = nl;                           // items of the current class (masked key == prefix)
-    // digits of 7 bits: bits 20..14, 13..7, 6..0
     for (int pass = 0; pass < 3; ++pass) {
-      const int shift = 14 - 7 * pass;
-      if (cls == need) break;                    // every item of the class is taken
-      for (int i = tid; i < 128; i += kThreads) hist[i] = 0;
-      __syncthreads();
-      for (uint32_t i = tid; i < nl; i += kThreads) {
-        const uint32_t key = list[i];
-        if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 127u], 1u);
+      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+      const uint32_t dmask = pass < 2 ? 2047u : 1023u;
+      if (pass > 0) {
+        for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kItems; ++u)
+          if (key[u] != 0u && (key[u] & pmask) == prefix) atomicAdd(&hist[(key[u] >> shift) & dmask], 1u);
+        __syncthreads();
       }
-      __syncthreads();
-      if (warp == 0) {
-        uint32_t cc[4], tt = 0;                  // lane l owns digits 127-4l .. 124-4l
-#pragma unroll
-        for (int u = 0; u < 4; ++u) { cc[u] = hist[127 - 4 * lane - u]; tt += cc[u]; }
-        uint32_t incl = tt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += x;
-        }
-        const uint32_t ex = incl - tt;
-        if (ex < need && need <= incl) {
-          uint32_t run = ex;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            if (run < need && need <= run + cc[u]) {
-              s_T = prefix | ((uint32_t)(127 - 4 * lane - u) << shift);
-              s_need = need - run;
-              s_cls = cc[u];
-            }
-            run += cc[u];
-          }
-        }
-      }
-      __syncthreads();
-      prefix = s_T;
-      need = s_need;
-      cls = s_cls;
-      pmask |= 127u << shift;
-      __syncthreads();
+      find_bin<kThreads>(hist, need, scr, res);
+      if (tid == 0) CSA_STAMP(5 + pass);
+      const uint32_t bin = res[0], cnt = res[2];
+      need = res[1];
+      prefix |= bin << shift;
+      pmask |= dmask << shift;
+      if (cnt == need) break;                                 // the whole class is taken
     }
-    // Keys of the final class: (key & pmask) == prefix. If the class was fully determined
-    // before the last pass (nl == need at some point), its members differ in their low bits;
-    // comparing the masked key keeps them together and all of them are taken.
-    T = prefix;
-    need_t = need;
   }
-  const uint32_t mask = pmask;
 
-  // ---- 3. order-preserving compaction: gt = (key & mask) > T, eq = (key & mask) == T
-  // warp w owns items [w*seg, (w+1)*seg), seg a multiple of 128; lane l takes 4 consecutive items
-  const int seg = ((n4 + kWarps - 1) / kWarps + 127) & ~127;
-  const int s0 = min(n4, warp * seg), s1 = min(n4, s0 + seg);
-  auto classify = [&](int i, uint32_t (&kq)[4], uint32_t& g, uint32_t& e) {
-    const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
-    kq[0] = v.x; kq[1] = v.y; kq[2] = v.z; kq[3] = v.w;
-    g = 0; e = 0;
+  // ---- order-preserving compaction of the winners
+  uint32_t ngt = 0, neq = 0;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const bool ok = kq[u] != 0u;
-      const uint32_t km = kq[u] & mask;
-      g |= (uint32_t)(ok && (take_all || km > T)) << u;
-      e |= (uint32_t)(ok && !take_all && km == T) << u;
-    }
-  };
-  uint32_t cg = 0, ce = 0;
-  for (int b = s0; b < s1; b += 128) {
-    const int i = b + 4 * lane;
-    if (i < s1) {
-      uint32_t kq[4], g, e;
-      classify(i, kq, g, e);
-      cg += __popc(g); ce += __popc(e);
-    }
+  for (int u = 0; u < kItems; ++u) {
+    const bool valid = key[u] != 0u;
+    const uint32_t m = key[u] & pmask;
+    ngt += valid && (take_all || m > prefix);
+    neq += valid && !take_all && m == prefix;
   }
-  cg = __reduce_add_sync(0xffffffffu, cg);
-  ce = __reduce_add_sync(0xffffffffu, ce);
-  if (lane == 0) { scr[warp] = cg; scr[64 + warp] = ce; }
-  __syncthreads();
-  uint32_t og = 0, oe = 0;
-  for (int w = 0; w < warp; ++w) { og += scr[w]; oe += scr[64 + w]; }
+  uint32_t rg, re, tgt, teq;
+  block_scan2<kThreads>(ngt, neq, scr, rg, re, tgt, teq);
+  if (tid == 0) CSA_STAMP(8);
   int32_t* out_final = p.topk ? p.topk + row * p.k : nullptr;
   const int64_t cand = row * ((int64_t)p.n_chunks * p.k) + (int64_t)blockIdx.x * p.k;
-  for (int b = s0; b < s1; b += 128) {
-    const int i = b + 4 * lane;
-    uint32_t kq[4] = {0, 0, 0, 0}, g = 0, e = 0;
-    if (i < s1) classify(i, kq, g, e);
-    // lane-exclusive prefix of the gt / eq counts
-    const uint32_t lg = __popc(g), le = __popc(e);
-    uint32_t ig = lg, ie = le;
+  const int64_t pf_row = (row / p.S) * p.pf_n_cap;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t xg = __shfl_up_sync(0xffffffffu, ig, o);
-      const uint32_t xe = __shfl_up_sync(0xffffffffu, ie, o);
-      if (lane >= o) { ig += xg; ie += xe; }
-    }
-    uint32_t rg = og + ig - lg, re = oe + ie - le;     // ranks of this lane's first item
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const bool gt = (g >> u) & 1u, eq = (e >> u) & 1u;
-      if (gt || (eq && re < need_t)) {
-        const uint32_t slot = rg + min(re, need_t);
-        const int32_t id = level0 ? (int32_t)(c0 + i + u) : idxs[i + u];
-        if (out_final) out_final[slot] = id;
-        else { p.out_key[cand + slot] = kq[u]; p.out_idx[cand + slot] = id; }
+  for (int u = 0; u < kItems; ++u) {
+    const bool valid = key[u] != 0u;
+    const uint32_t m = key[u] & pmask;
+    const bool gt = valid && (take_all || m > prefix);
+    const bool eq = valid && !take_all && m == prefix;
+    if (gt || (eq && re < need)) {
+      const uint32_t slot = rg + min(re, need);
+      if (out_final) {
+        out_final[slot] = id[u];
+        if (p.pf_ckv) prefetch_l2(p.pf_ckv + (pf_row + id[u]) * p.pf_row_bytes, p.pf_row_bytes);
+      } else {
+        p.out_key[cand + slot] = key[u];
+        p.out_idx[cand + slot] = id[u];
       }
-      rg += gt;
-      re += eq;
     }
-    og += __shfl_sync(0xffffffffu, ig, 31);
-    oe += __shfl_sync(0xffffffffu, ie, 31);
+    rg += gt;
+    re += eq;
   }
-  // unused slots
-  for (int j = kk + tid; j < p.k; j += kThreads) {
+  for (int j = (int)kk + tid; j < p.k; j += kThreads) {
     if (out_final) out_final[j] = -1;
     else { p.out_key[cand + j] = 0u; p.out_idx[cand + j] = -1; }
+  }
+  if (tid == 0) CSA_STAMP(9);
+  // ---- the attention reads this query's window and q next: ask L2 for them now
+  if (p.topk && p.pf_kv && blockIdx.x == 0) {
+    const int64_t t = p.pos ? p.pos[row] : (row % p.S);
+    const int64_t lo = t - p.pf_window + 1 > 0 ? t - p.pf_window + 1 : 0;
+    const uint8_t* w0 = p.pf_kv + ((row / p.S) * p.pf_N + lo) * p.pf_row_bytes;
+    for (int64_t r = tid; r < t - lo + 1; r += kThreads) prefetch_l2(w0 + r * p.pf_row_bytes, p.pf_row_bytes);
+    for (int q = tid; q * 4096 < p.pf_q_bytes; q += kThreads)
+      prefetch_l2(p.pf_q + row * (int64_t)p.pf_q_bytes + q * 4096, min(4096, p.pf_q_bytes - q * 4096));
   }
 }
 
 template <int kThreads>
-cudaError_t launch_select(const SelParams& p, int64_t rows, int cap, cudaStream_t st, bool pdl) {
-  const bool with_idx = p.scores == nullptr;
-  const size_t smem = SelSmem<kThreads>::bytes(cap, with_idx);
+cudaError_t launch_select(const SelParams& p, int64_t rows, cudaStream_t st, bool pdl) {
+  const size_t smem = SelSmem<kThreads>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(topk_select_kernel<kThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.n_chunks, (unsigned)rows);
-  return launch_kernel(pdl, topk_select_kernel<kThreads>, grid, dim3(kThreads), smem, st, p, cap);
+  return launch_kernel(pdl, topk_select_kernel<kThreads>, grid, dim3(kThreads), smem, st, p);
 }
 
-// Items one CTA holds: the large variant (1024 threads) serves the later levels of very long rows;
-// the small one (512 threads for decode rows, 256 for the many short rows of a prefill) the first
-// level and every short row. Cutting decode rows into 4096-entry chunks spreads the first level
-// over many SMs; its winners (k per chunk) are then few enough for one small CTA per row.
-constexpr int kCapLarge = 16384;
-constexpr int kCapSmall = 4096;
+constexpr int kCapLarge = 1024 * kItems;     // 16384 items: one CTA of 1024 threads
+constexpr int kCapMid = 256 * kItems;        // 4096
+constexpr int kCapSmall = 128 * kItems;      // 2048
 
 }  // namespace
+
+// A row longer than one small CTA is first cut into 2048-item chunks, one 128-thread CTA each: one
+// SM moves only tens of GB/s, so spreading the first pass over many SMs is what makes it fast. The
+// chunks' winners (k per chunk, in index order) then go through further levels (16384-item chunks
+// while more than 16384 remain) until one CTA holds a row.
+static int64_t first_level_chunks(int64_t n_cap) { return (n_cap + kCapSmall - 1) / kCapSmall; }
 
 size_t topk_workspace_bytes(int64_t rows, int64_t n_cap, int k) {
   // candidates of the intermediate levels: two ping-pong buffers of (key, index) pairs, each large
   // enough for the first level's output
   if (n_cap <= kCapSmall || k <= 0) return 0;
-  const int64_t chunks = (n_cap + kCapSmall - 1) / kCapSmall;
-  return 2 * (size_t)rows * chunks * k * 8;
+  return 2 * (size_t)rows * first_level_chunks(n_cap) * k * 8;
 }
 
 cudaError_t launch_topk(int B, const TopkParams& p, cudaStream_t st, bool pdl) {
@@ -346,22 +316,24 @@ cudaError_t launch_topk(int B, const TopkParams& p, cudaStream_t st, bool pdl) {
   SelParams s;
   s.scores = p.scores; s.in_key = nullptr; s.in_idx = nullptr; s.n_in = p.n_cap; s.pos = p.pos;
   s.S = p.S; s.ratio = p.ratio; s.k = p.k;
+  s.pf_ckv = nullptr; s.pf_kv = nullptr; s.pf_q = nullptr;
+  s.pf_n_cap = p.pf_n_cap; s.pf_N = p.pf_N; s.pf_row_bytes = p.pf_row_bytes; s.pf_window = p.pf_window;
+  s.pf_q_bytes = p.pf_q_bytes;
   uint8_t* ws = static_cast<uint8_t*>(p.ws);
   const size_t half = topk_workspace_bytes(rows, p.n_cap, p.k) / 2;
   int64_t n_in = p.n_cap;
   for (int level = 0;; ++level) {
-    const bool first_launch = level == 0;
-    const bool dep = pdl || !first_launch;
-    if (n_in <= kCapSmall) {                                   // one small CTA holds the row: final level
-      s.chunk = (int)((n_in + 3) & ~3ll); s.n_chunks = 1;
+    const bool dep = pdl || level > 0;
+    const bool fits = n_in <= kCapSmall || (level > 0 && n_in <= kCapLarge);
+    if (fits) {                                                // one CTA holds the row: final level
+      s.chunk = (int)n_in; s.n_chunks = 1;
       s.topk = p.topk; s.out_key = nullptr; s.out_idx = nullptr;
-      if (p.S > 1) return launch_select<256>(s, rows, kCapSmall, st, dep);
-      return launch_select<512>(s, rows, kCapSmall, st, dep);
-    }
-    if (level > 0 && n_in <= kCapLarge) {                      // one large CTA holds the row: final level
-      s.chunk = (int)((n_in + 3) & ~3ll); s.n_chunks = 1;
-      s.topk = p.topk; s.out_key = nullptr; s.out_idx = nullptr;
-      return launch_select<1024>(s, rows, kCapLarge, st, dep);
+      s.pf_ckv = static_cast<const uint8_t*>(p.pf_ckv);
+      s.pf_kv = static_cast<const uint8_t*>(p.pf_kv);
+      s.pf_q = static_cast<const uint8_t*>(p.pf_q);
+      if (n_in <= kCapSmall) return launch_select<128>(s, rows, st, dep);
+      if (n_in <= kCapMid) return launch_select<256>(s, rows, st, dep);
+      return launch_select<1024>(s, rows, st, dep);
     }
     if (!ws) return cudaErrorInvalidValue;
     const int64_t cap = level == 0 ? kCapSmall : kCapLarge;
@@ -372,8 +344,7 @@ cudaError_t launch_topk(int B, const TopkParams& p, cudaStream_t st, bool pdl) {
     s.topk = nullptr;
     s.out_key = reinterpret_cast<uint32_t*>(buf);
     s.out_idx = reinterpret_cast<int32_t*>(buf + (size_t)rows * n_out * 4);
-    cudaError_t e = level == 0 ? launch_select<512>(s, rows, kCapSmall, st, dep)
-                               : launch_select<1024>(s, rows, kCapLarge, st, dep);
+    cudaError_t e = level == 0 ? launch_select<128>(s, rows, st, dep) : launch_select<1024>(s, rows, st, dep);
     if (e != cudaSuccess) return e;
     s.scores = nullptr; s.pos = nullptr;
     s.in_key = s.out_key; s.in_idx = s.out_idx; s.n_in = n_out;

@@ -23,6 +23,9 @@ DECODE = {
                      [4098 - 37 * b for b in range(32)]),
     "hca_bf16_B16_wide": (synth.small_workload(3, wid=105, B=16, N=19215, t=19214, ratio=16),
                           [19214, 19199] + [19214 - 977 * b for b in range(2, 16)]),
+    # more tiles than two waves of CTAs: two tiles per CTA, one of them gathered twice
+    "csa_bf16_B64": (synth.small_workload(1, wid=106, B=64, N=2051, t=2050),
+                     [2050 - 13 * b for b in range(64)]),
 }
 MODES = [False, True]          # tensor-core path where available, then the CUDA-core path
 
