@@ -259,8 +259,7 @@ csa_status run_compress(const csa_config* c, int B, const csa_cache* k, int64_t 
 
 csa_status run_index_topk(const csa_config* c, int B, int S, const int64_t* pos, const void* q_idx,
                           const float* w, const void* cidx, int64_t n_cap, int32_t* topk,
-                          float* scores, void* tk_ws, void* tc_ws, cudaStream_t st, bool pdl,
-                          const csa_cache* pf_cache = nullptr, const void* pf_q = nullptr) {
+                          float* scores, void* tk_ws, void* tc_ws, cudaStream_t st, bool pdl) {
   const bool bf16 = c->storage == CSA_BF16;
   if (use_tc_index(c)) {
     const RopeTab rope = make_rope(c);
@@ -281,16 +280,6 @@ csa_status run_index_topk(const csa_config* c, int B, int S, const int64_t* pos,
   TopkParams tp;
   tp.scores = scores; tp.topk = topk; tp.pos = pos; tp.n_cap = n_cap; tp.S = S; tp.k = c->top_k;
   tp.ratio = c->ratio; tp.ws = tk_ws;
-  // decode: the selection also asks L2 for the rows the attention reads next
-  const int es = c->storage == CSA_BF16 ? 2 : 4;
-  tp.pf_ckv = pf_cache ? pf_cache->ckv : nullptr;
-  tp.pf_kv = pf_cache ? pf_cache->kv : nullptr;
-  tp.pf_q = pf_cache ? pf_q : nullptr;
-  tp.pf_n_cap = pf_cache ? pf_cache->n_cap : 0;
-  tp.pf_N = pf_cache ? pf_cache->N : 0;
-  tp.pf_row_bytes = c->d * es;
-  tp.pf_window = c->window;
-  tp.pf_q_bytes = c->H * c->d * es;
   return cuda_status(launch_stage(ST_TOPK, st, [&] { return launch_topk(B, tp, st, true); }), "top-k launch");
 }
 
@@ -469,7 +458,7 @@ csa_status csa_decode(const csa_config* cfg, int32_t B, const int64_t* pos, cons
     tk = topk_out ? topk_out : carve<int32_t>(ws, pl.off_topk);
     s = run_index_topk(cfg, B, 1, pos, q_idx, w, cache->cidx, cache->n_cap, tk,
                        carve<float>(ws, pl.off_scores), carve<char>(ws, pl.off_tksel), carve<char>(ws, pl.off_tc),
-                       stream, true, cache, q);
+                       stream, true);
     if (s != CSA_OK) return s;
   }
   return run_attn(cfg, pl, B, 1, pos, q, cache->kv, cache->N, cache->ckv, cache->n_cap, tk, sink, out, ws,

@@ -208,6 +208,7 @@ constexpr int kMergeBatch = 4;
 
 template <typename T>
 __global__ void __launch_bounds__(32 * kMergeHeads) attn_merge_kernel(const AttnParams p) {
+  if (threadIdx.x == 0) CSA_STAMP(50);
   griddep_launch();
   griddep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -287,6 +288,7 @@ __global__ void __launch_bounds__(32 * kMergeHeads) attn_merge_kernel(const Attn
   for (int k = 0; k < 8; ++k) { a8[k] = acc[k]; b8[k] = acc[8 + k]; }
   store8(op, a8);
   store8(op + 8, b8);
+  if (threadIdx.x == 0) CSA_STAMP(51);
 }
 
 }  // namespace

@@ -254,11 +254,13 @@ __device__ void compress_close(const CompressParams& p, const CompressJob& job, 
 template <typename T>
 __global__ void __launch_bounds__(kCloseThreads) compress_close_kernel(const CompressParams p) {
   extern __shared__ float sm[];
+  if (threadIdx.x == 0) CSA_STAMP(40);
   griddep_launch();
   griddep_wait();
   const CompressJob& job = p.job[blockIdx.y];
   if (job.C == 512) compress_close<T, 512>(p, job, sm);
   else compress_close<T, 128>(p, job, sm);
+  if (threadIdx.x == 0) CSA_STAMP(41);
 }
 
 }  // namespace

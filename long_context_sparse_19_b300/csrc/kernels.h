@@ -52,13 +52,6 @@ struct TopkParams {
   int64_t n_cap;
   int S, k, ratio;
   void* ws;              // candidate buffers of the multi-level selection (topk_workspace_bytes)
-  // Optional L2 prefetch of what the attention will read next (all null / 0: none): the selected
-  // rows of ckv [B, n_cap, row_bytes], the raw window rows of kv [B, N, row_bytes] and q rows.
-  const void* pf_ckv;
-  const void* pf_kv;
-  const void* pf_q;
-  int64_t pf_n_cap, pf_N;
-  int pf_row_bytes, pf_window, pf_q_bytes;
 };
 
 size_t topk_workspace_bytes(int64_t rows, int64_t n_cap, int k);

@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     rows_s[i] = (int32_t)g;
     // the gathers below are limited by how many requests one SM keeps in flight: have L2 fetch
-    // every row of the CTA at once (a no-op when the selection kernel already asked for it)
+    // every row of the CTA at once
     if (g >= 0) prefetch_l2((tid_ < p.win_tiles ? p.kv : p.ckv) + g * kD, kD * 2);
   }
   __syncthreads();

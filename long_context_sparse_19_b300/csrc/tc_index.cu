@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
   float* w_s = reinterpret_cast<float*>(tmem_slot + 4);    // [64]
 
+  if (threadIdx.x == 0) CSA_STAMP(42);
   griddep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z, s = blockIdx.y;
@@ -165,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       store8(reinterpret_cast<__nv_bfloat16*>(qop + blk * kBlockBytes + sw128_offset(64 + h, ch)), lo);
     }
     if (et < 64) w_s[et] = wv;
+    if (et == 0) CSA_STAMP(43);
     fence_proxy_async_smem();
     mbar_arrive(qready);
     named_barrier(1, 128);                                  // w_s visible to every epilogue thread
@@ -196,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) CSA_STAMP(44);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

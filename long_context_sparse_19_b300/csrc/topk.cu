@@ -42,12 +42,6 @@ struct SelParams {
   int32_t* topk;             // final level: [rows, k], ascending entry index, -1 padded
   uint32_t* out_key;         // otherwise: [rows, n_chunks * k] candidates (-1 padded)
   int32_t* out_idx;
-  // final level only, optional: L2 prefetch of the selected ckv rows, the window and the q rows
-  const uint8_t* pf_ckv;
-  const uint8_t* pf_kv;
-  const uint8_t* pf_q;
-  int64_t pf_n_cap, pf_N;
-  int pf_row_bytes, pf_window, pf_q_bytes;
 };
 
 template <int kThreads>
@@ -120,10 +114,11 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const SelParams p
   uint32_t* scr = hist + kBins;                                     // [128]
   uint32_t* res = scr + 128;                                        // [16]
 
-  if (threadIdx.x == 0) CSA_STAMP(0);
+  if (threadIdx.x == 0) CSA_STAMP(54);
+  if (threadIdx.x == 0) CSA_STAMP(gridDim.x > 1 ? 45 : 47);
   griddep_launch();
   griddep_wait();
-  if (threadIdx.x == 0) CSA_STAMP(1);
+  if (threadIdx.x == 0) CSA_STAMP(55);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.y;
   const int64_t c0 = (int64_t)blockIdx.x * p.chunk;
@@ -166,7 +161,7 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const SelParams p
   }
 
   // ---- first digit (key bits 31..21): per-warp private histograms, then summed
-  if (tid == 0) CSA_STAMP(2);
+  if (tid == 0) CSA_STAMP(56);
   {
     uint4* z = reinterpret_cast<uint4*>(whist);
     for (int i = tid; i < kWarps * (kBins / 2) / 4; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
@@ -188,7 +183,7 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const SelParams p
     if (lane == 0 && nv) atomicAdd(&res[8], nv);
   }
   __syncthreads();
-  if (tid == 0) CSA_STAMP(3);
+  if (tid == 0) CSA_STAMP(57);
   for (int b2 = tid; b2 < kBins / 2; b2 += kThreads) {
     uint32_t lo = 0, hi = 0;
 #pragma unroll 4
@@ -201,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const SelParams p
     hist[2 * b2 + 1] = hi;
   }
   __syncthreads();
-  if (tid == 0) CSA_STAMP(4);
+  if (tid == 0) CSA_STAMP(58);
   const uint32_t n_valid = res[8];
   const uint32_t kk = min((uint32_t)p.k, n_valid);
   const bool take_all = kk >= n_valid;
@@ -222,7 +217,7 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const SelParams p
         __syncthreads();
       }
       find_bin<kThreads>(hist, need, scr, res);
-      if (tid == 0) CSA_STAMP(5 + pass);
+      if (tid == 0) CSA_STAMP(59 + pass);
       const uint32_t bin = res[0], cnt = res[2];
       need = res[1];
       prefix |= bin << shift;
@@ -242,10 +237,9 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const SelParams p
   }
   uint32_t rg, re, tgt, teq;
   block_scan2<kThreads>(ngt, neq, scr, rg, re, tgt, teq);
-  if (tid == 0) CSA_STAMP(8);
+  if (tid == 0) CSA_STAMP(62);
   int32_t* out_final = p.topk ? p.topk + row * p.k : nullptr;
   const int64_t cand = row * ((int64_t)p.n_chunks * p.k) + (int64_t)blockIdx.x * p.k;
-  const int64_t pf_row = (row / p.S) * p.pf_n_cap;
 #pragma unroll
   for (int u = 0; u < kItems; ++u) {
     const bool valid = key[u] != 0u;
@@ -256,7 +250,6 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const SelParams p
       const uint32_t slot = rg + min(re, need);
       if (out_final) {
         out_final[slot] = id[u];
-        if (p.pf_ckv) prefetch_l2(p.pf_ckv + (pf_row + id[u]) * p.pf_row_bytes, p.pf_row_bytes);
       } else {
         p.out_key[cand + slot] = key[u];
         p.out_idx[cand + slot] = id[u];
@@ -269,16 +262,300 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const SelParams p
     if (out_final) out_final[j] = -1;
     else { p.out_key[cand + j] = 0u; p.out_idx[cand + j] = -1; }
   }
-  if (tid == 0) CSA_STAMP(9);
-  // ---- the attention reads this query's window and q next: ask L2 for them now
-  if (p.topk && p.pf_kv && blockIdx.x == 0) {
+  if (tid == 0) CSA_STAMP(63);
+  if (tid == 0) CSA_STAMP(gridDim.x > 1 ? 46 : 48);
+}
+
+// ------------------------------------------------------------------ one row, one cluster
+// A row of up to 8 x 2048 items is selected by one thread-block cluster in a single launch. CTA r
+// of the cluster holds items 2048 r .. 2048 r + 2047 (16 per thread, in registers). The CTAs share
+// what they find by writing into each other's shared memory (remote adds and stores: no round
+// trips) followed by a cluster barrier. Remote requests are slow one by one, so each CTA sends as
+// few as it can:
+//   1. every CTA adds its histogram of the keys' top 11 bits into every CTA's copy of the cluster
+//      histogram, but only from the bin of its own k-th largest key upwards: the row's k-th largest
+//      key is at least as large, so the bins below cannot hold it. After the barrier each CTA finds
+//      the same threshold bin (a bin of more than kListCap items is first refined by the next 11
+//      bits through another exchange);
+//   2. every CTA stores its counts of items above the bin and in it into every CTA, and, when the
+//      bin must be split, its in-bin keys in index order; after the barrier every CTA holds the
+//      bin's keys in row order and finds the last digits of the threshold on its own;
+// then every CTA writes its winners in ascending index order. No CTA writes to another after the
+// last barrier it takes part in, so none can exit while another still writes to it. Shared memory
+// is kept near 40 KB: a larger footprint delays placing the 8-CTA clusters beside the indexer and
+// attention CTAs of neighbouring launches, which costs more than the rarer second exchange saves.
+constexpr int kCluThreads = 128;
+constexpr int kCluChunk = kCluThreads * kItems;          // 2048 items per CTA
+constexpr int kCluMax = 8;                                // portable cluster size
+constexpr int kListCap = 256;                             // in-bin items split locally (cluster total)
+constexpr int kListPer = kListCap / kCluThreads;          // list positions per thread in the final order
+static_assert(kListCap % kCluThreads == 0, "the final order gives each thread the same number of list positions");
+
+struct CluSmem {
+  uint32_t full[3][kBins];              // cluster histogram of each digit pass (remote adds)
+  uint32_t hist[kBins];                 // this CTA's histogram; later the local digit passes
+  uint32_t list[kCluMax][kListCap];     // in-bin keys of each source CTA, index order (remote stores)
+  uint32_t all_list[kListCap];          // the same, concatenated in row order
+  uint32_t src_cnt[kCluMax][2];         // per source CTA: (items above the bin, in it) (remote stores)
+  uint32_t n_valid;                     // the row's valid items (remote adds)
+  uint32_t scr[64];
+  uint32_t res[4];
+  uint8_t taken[kListCap];              // in-bin item (row order) is selected
+};
+
+__global__ void __launch_bounds__(kCluThreads) topk_cluster_kernel(const SelParams p) {
+  extern __shared__ __align__(16) uint8_t clu_raw[];
+  CluSmem& sm = *reinterpret_cast<CluSmem*>(clu_raw);
+  if (threadIdx.x == 0) CSA_STAMP(47);
+  const int tid = threadIdx.x, lane = tid & 31;
+  const uint32_t rank = cluster_rank(), C = gridDim.x;
+  for (int i = tid; i < 3 * kBins; i += kCluThreads) (&sm.full[0][0])[i] = 0;
+  if (tid == 0) sm.n_valid = 0;
+  cluster_arrive();                                       // the zeroed counters may be added into
+  griddep_launch();
+  griddep_wait();
+  if (tid == 0) CSA_STAMP(54);
+  const int64_t row = blockIdx.y;
+  const int64_t c0 = (int64_t)rank * kCluChunk;
+  const bool level0 = p.scores != nullptr;
+  int n;
+  if (level0) {
     const int64_t t = p.pos ? p.pos[row] : (row % p.S);
-    const int64_t lo = t - p.pf_window + 1 > 0 ? t - p.pf_window + 1 : 0;
-    const uint8_t* w0 = p.pf_kv + ((row / p.S) * p.pf_N + lo) * p.pf_row_bytes;
-    for (int64_t r = tid; r < t - lo + 1; r += kThreads) prefetch_l2(w0 + r * p.pf_row_bytes, p.pf_row_bytes);
-    for (int q = tid; q * 4096 < p.pf_q_bytes; q += kThreads)
-      prefetch_l2(p.pf_q + row * (int64_t)p.pf_q_bytes + q * 4096, min(4096, p.pf_q_bytes - q * 4096));
+    const int64_t V = t < 0 ? 0 : min(visible_entries(t, p.ratio), p.n_in);
+    n = (int)max((int64_t)0, min((int64_t)kCluChunk, V - c0));
+  } else {
+    n = (int)max((int64_t)0, min((int64_t)kCluChunk, p.n_in - c0));
   }
+  uint32_t key[kItems];
+  int32_t id[kItems];
+  const int i0 = tid * kItems;
+  if (level0) {
+    const float* sc = p.scores + row * p.n_in + c0 + i0;
+    if (((row * p.n_in + c0) & 3) == 0 && i0 + kItems <= n) {
+#pragma unroll
+      for (int q = 0; q < kItems / 4; ++q) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(sc) + q);
+        key[4 * q] = order_key(f.x); key[4 * q + 1] = order_key(f.y);
+        key[4 * q + 2] = order_key(f.z); key[4 * q + 3] = order_key(f.w);
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kItems; ++u) key[u] = i0 + u < n ? order_key(__ldg(sc + u)) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) id[u] = (int32_t)(c0 + i0 + u);
+  } else {
+    const uint32_t* ik = p.in_key + row * p.n_in + c0 + i0;
+    const int32_t* ii = p.in_idx + row * p.n_in + c0 + i0;
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) id[u] = i0 + u < n ? __ldg(ii + u) : -1;
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) key[u] = id[u] >= 0 ? __ldg(ik + u) : 0u;
+  }
+
+
+  if (tid == 0) CSA_STAMP(55);
+  // ---- threshold class: digits of 11, 11, 10 bits over the cluster's summed histograms
+  uint32_t prefix = 0, pmask = 0, need = 0, n_valid = 0, class_cnt = 0;
+  bool take_all = false;
+  int pass = 0;
+  for (; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const uint32_t dmask = pass < 2 ? 2047u : 1023u;
+    for (int i = tid; i < kBins; i += kCluThreads) sm.hist[i] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kItems; ++u)
+      if (key[u] != 0u && (key[u] & pmask) == prefix) atomicAdd(&sm.hist[(key[u] >> shift) & dmask], 1u);
+    __syncthreads();
+    uint32_t floor_bin = 0;                               // bins below it are not sent
+    if (pass == 0) {
+      uint32_t nl = 0;
+#pragma unroll
+      for (int u = 0; u < kItems; ++u) nl += key[u] != 0u;
+      uint32_t d0, d1, d2;
+      block_scan2<kCluThreads>(nl, 0u, sm.scr, d0, d1, nl, d2);   // this CTA's valid items
+      if (nl > (uint32_t)p.k) {
+        find_bin<kCluThreads>(sm.hist, (uint32_t)p.k, sm.scr, sm.res);
+        floor_bin = sm.res[0];
+      }
+      cluster_wait();                                     // every CTA has zeroed its counters
+      if (tid < (int)C && nl != 0u) dsmem_add(dsmem_addr(&sm.n_valid, (uint32_t)tid), nl);
+      if (tid == 0) CSA_STAMP(56);
+    } else if (tid == 0) {
+      CSA_STAMP(52);
+    }
+    for (int i = tid; i < kBins; i += kCluThreads) {
+      const uint32_t v = sm.hist[i];
+      if (v != 0u && (uint32_t)i >= floor_bin)
+        for (uint32_t r = 0; r < C; ++r) dsmem_add(dsmem_addr(&sm.full[pass][i], r), v);
+    }
+    cluster_sync();                                       // every CTA's additions have landed
+    if (tid == 0) CSA_STAMP(pass == 0 ? 57 : 53);
+    if (pass == 0) {
+      n_valid = sm.n_valid;
+      need = min((uint32_t)p.k, n_valid);
+      take_all = need >= n_valid;
+      if (take_all) break;
+    }
+    find_bin<kCluThreads>(sm.full[pass], need, sm.scr, sm.res);
+    prefix |= sm.res[0] << shift;
+    pmask |= dmask << shift;
+    need = sm.res[1];
+    class_cnt = sm.res[2];
+    __syncthreads();                                      // res is written again by the next search
+    if (tid == 0) CSA_STAMP(58 + pass);
+    if (class_cnt == need || class_cnt <= kListCap) break;   // wholly taken, or split locally
+  }
+  const uint32_t kk = min((uint32_t)p.k, n_valid);
+
+  // ---- this CTA's items above the class and in it, and their offsets within the CTA
+  uint32_t ngt = 0, neq = 0;
+#pragma unroll
+  for (int u = 0; u < kItems; ++u) {
+    const bool valid = key[u] != 0u;
+    const uint32_t m = key[u] & pmask;
+    ngt += valid && (take_all || m > prefix);
+    neq += valid && !take_all && m == prefix;
+  }
+  uint32_t rg, re, GT, EQ;
+  block_scan2<kCluThreads>(ngt, neq, sm.scr, rg, re, GT, EQ);
+  // the class is split locally when only part of it is taken and digits remain (the same in every CTA)
+  const bool split = !take_all && class_cnt > need && pmask != 0xFFFFFFFFu;
+  if (tid < (int)C) {
+    const uint32_t at = dsmem_addr(&sm.src_cnt[rank][0], (uint32_t)tid);
+    dsmem_st(at, GT);
+    dsmem_st(at + 4, EQ);
+  }
+  if (split) {                                            // class_cnt <= kListCap here
+    uint32_t e = re;
+#pragma unroll
+    for (int u = 0; u < kItems; ++u)
+      if (key[u] != 0u && (key[u] & pmask) == prefix) {
+        for (uint32_t r = 0; r < C; ++r) dsmem_st(dsmem_addr(&sm.list[rank][e], r), key[u]);
+        ++e;
+      }
+  }
+  if (tid == 0) CSA_STAMP(61);
+  cluster_sync();                                         // counts and lists have landed: the last barrier
+  uint32_t gt_off = 0, eq_off = 0, eq_total = 0;
+  for (uint32_t r = 0; r < C; ++r) {
+    if (r < rank) { gt_off += sm.src_cnt[r][0]; eq_off += sm.src_cnt[r][1]; }
+    eq_total += sm.src_cnt[r][1];
+  }
+  const bool all_eq_taken = take_all || eq_total <= need;
+  const bool by_position = !all_eq_taken && !split;       // all 32 bits fixed: equal keys, first `need`
+  if (split) {
+    for (uint32_t gpos = tid; gpos < eq_total; gpos += kCluThreads) {
+      uint32_t r = 0, base = 0;
+      while (r + 1 < C && gpos >= base + sm.src_cnt[r][1]) { base += sm.src_cnt[r][1]; ++r; }
+      sm.all_list[gpos] = sm.list[r][gpos - base];
+    }
+    __syncthreads();
+    // the remaining digits of the threshold, over the class's keys only
+    uint32_t lp = prefix, lm = pmask, ln = need;
+    for (int dp = pass + 1; dp < 3; ++dp) {
+      const int shift = dp == 1 ? 10 : 0;
+      const uint32_t dmask = dp == 1 ? 2047u : 1023u;
+      for (int i = tid; i < kBins; i += kCluThreads) sm.hist[i] = 0;
+      __syncthreads();
+      for (uint32_t gpos = tid; gpos < eq_total; gpos += kCluThreads) {
+        const uint32_t kv = sm.all_list[gpos];
+        if ((kv & lm) == lp) atomicAdd(&sm.hist[(kv >> shift) & dmask], 1u);
+      }
+      __syncthreads();
+      find_bin<kCluThreads>(sm.hist, ln, sm.scr, sm.res);
+      lp |= sm.res[0] << shift;
+      lm |= dmask << shift;
+      ln = sm.res[1];
+      const uint32_t cls = sm.res[2];
+      __syncthreads();
+      if (cls == ln) break;
+    }
+    // taken: above the final class, or in it and among its first `ln` in row order
+    const uint32_t q0 = kListPer * tid;
+    uint32_t c = 0;
+#pragma unroll
+    for (int j = 0; j < kListPer; ++j)
+      c += q0 + j < eq_total && (sm.all_list[q0 + j] & lm) == lp;
+    uint32_t ce, d0, d1, d2;
+    block_scan2<kCluThreads>(c, 0u, sm.scr, ce, d0, d1, d2);
+#pragma unroll
+    for (int j = 0; j < kListPer; ++j)
+      if (q0 + j < eq_total) {
+        const uint32_t m = sm.all_list[q0 + j] & lm;
+        sm.taken[q0 + j] = m > lp || (m == lp && ce++ < ln);
+      }
+    __syncthreads();
+    if (tid == 0) CSA_STAMP(62);
+  }
+  auto eq_taken = [&](uint32_t gpos) -> bool {
+    return all_eq_taken ? true : (by_position ? gpos < need : sm.taken[gpos] != 0);
+  };
+  // taken in-bin items of the CTAs before this one
+  uint32_t tb = 0;
+  if (all_eq_taken) tb = eq_off;
+  else if (by_position) tb = min(eq_off, need);
+  else {
+    uint32_t c = 0;
+    for (uint32_t gpos = tid; gpos < eq_off; gpos += kCluThreads) c += sm.taken[gpos];
+    c = __reduce_add_sync(0xffffffffu, c);
+    if (lane == 0) sm.scr[tid >> 5] = c;
+    __syncthreads();
+    for (int w = 0; w < kCluThreads / 32; ++w) tb += sm.scr[w];
+    __syncthreads();
+  }
+  if (tid == 0) CSA_STAMP(63);
+  // ---- write the winners in ascending index order
+  uint32_t mine = ngt;
+  {
+    uint32_t e = eq_off + re;
+#pragma unroll
+    for (int u = 0; u < kItems; ++u)
+      if (key[u] != 0u && !take_all && (key[u] & pmask) == prefix) mine += eq_taken(e++);
+  }
+  uint32_t wex, d2, wtot, d3;
+  block_scan2<kCluThreads>(mine, 0u, sm.scr, wex, d2, wtot, d3);
+  uint32_t slot = gt_off + tb + wex;
+  uint32_t e = eq_off + re;
+  int32_t* out = p.topk + row * p.k;
+#pragma unroll
+  for (int u = 0; u < kItems; ++u) {
+    const bool valid = key[u] != 0u;
+    const uint32_t m = key[u] & pmask;
+    const bool gt = valid && (take_all || m > prefix);
+    const bool eq = valid && !take_all && m == prefix;
+    bool t_ = gt;
+    if (eq) t_ = eq_taken(e++);
+    if (t_) out[slot++] = id[u];
+  }
+  for (int j = (int)kk + (int)(rank * kCluThreads) + tid; j < p.k; j += (int)(C * kCluThreads)) out[j] = -1;
+  if (tid == 0) CSA_STAMP(48);
+}
+
+cudaError_t launch_cluster_select(const SelParams& p, int64_t rows, int C, cudaStream_t st, bool pdl) {
+  cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sizeof(CluSmem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)C, (unsigned)rows);
+  cfg.blockDim = dim3(kCluThreads);
+  cfg.dynamicSmemBytes = sizeof(CluSmem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  int na = 1;
+  if (pdl) {
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    na = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, topk_cluster_kernel, p);
 }
 
 template <int kThreads>
@@ -316,22 +593,18 @@ cudaError_t launch_topk(int B, const TopkParams& p, cudaStream_t st, bool pdl) {
   SelParams s;
   s.scores = p.scores; s.in_key = nullptr; s.in_idx = nullptr; s.n_in = p.n_cap; s.pos = p.pos;
   s.S = p.S; s.ratio = p.ratio; s.k = p.k;
-  s.pf_ckv = nullptr; s.pf_kv = nullptr; s.pf_q = nullptr;
-  s.pf_n_cap = p.pf_n_cap; s.pf_N = p.pf_N; s.pf_row_bytes = p.pf_row_bytes; s.pf_window = p.pf_window;
-  s.pf_q_bytes = p.pf_q_bytes;
   uint8_t* ws = static_cast<uint8_t*>(p.ws);
   const size_t half = topk_workspace_bytes(rows, p.n_cap, p.k) / 2;
   int64_t n_in = p.n_cap;
   for (int level = 0;; ++level) {
     const bool dep = pdl || level > 0;
-    const bool fits = n_in <= kCapSmall || (level > 0 && n_in <= kCapLarge);
+    const bool fits = n_in <= (int64_t)kCluMax * kCluChunk || (level > 0 && n_in <= kCapLarge);
     if (fits) {                                                // one CTA holds the row: final level
       s.chunk = (int)n_in; s.n_chunks = 1;
       s.topk = p.topk; s.out_key = nullptr; s.out_idx = nullptr;
-      s.pf_ckv = static_cast<const uint8_t*>(p.pf_ckv);
-      s.pf_kv = static_cast<const uint8_t*>(p.pf_kv);
-      s.pf_q = static_cast<const uint8_t*>(p.pf_q);
       if (n_in <= kCapSmall) return launch_select<128>(s, rows, st, dep);
+      if (n_in <= (int64_t)kCluMax * kCluChunk)                // one cluster of 2048-item CTAs per row
+        return launch_cluster_select(s, rows, (int)((n_in + kCluChunk - 1) / kCluChunk), st, dep);
       if (n_in <= kCapMid) return launch_select<256>(s, rows, st, dep);
       return launch_select<1024>(s, rows, st, dep);
     }

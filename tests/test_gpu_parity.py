@@ -300,3 +300,41 @@ def test_topk_long_rows_exact(n_cap, k, B, dup):
         Hn.check_topk_exact(tk, got, k, f"long row b{b}")
         ref = O.index_scores(q_idx[b, 0], w[b, 0], cidx[b], t, 4)
         Hn.check_scores(got, ref, "bf16", f"long row scores b{b}")
+
+
+@pytest.mark.parametrize("n_cap", [16384, 6000])
+@pytest.mark.parametrize("mode", ["equal", "narrow", "few"])
+def test_topk_one_cluster_paths(n_cap, mode):
+    """Rows of 2049..16384 entries are selected by one cluster of CTAs. Score distributions that
+    force each of its paths: every score equal (all digits exchanged, then the first k by
+    position), scores packed into a narrow range (the threshold bin holds more than the in-bin list
+    takes, so a further digit is exchanged before the bin is split locally), and few distinct
+    values (large groups of exact ties). The selection must equal the exact (-score, index)
+    selection of the GPU's own scores."""
+    rng = np.random.default_rng(n_cap + len(mode))
+    import synth as S
+    L = Hn.lib()
+    B, H_idx, k = 2, 64, 512
+    base = rng.standard_normal((1, 1, 128), dtype=np.float32) / np.float32(np.sqrt(128))
+    if mode == "equal":
+        cidx = np.repeat(np.repeat(base, n_cap, axis=1), B, axis=0)
+    elif mode == "narrow":
+        cidx = base + np.float32(2e-3) * rng.standard_normal((B, n_cap, 128), dtype=np.float32)
+    else:
+        rows = rng.standard_normal((B, 37, 128), dtype=np.float32) / np.float32(np.sqrt(128))
+        cidx = rows[:, rng.integers(0, 37, n_cap)]
+    cidx = S.round_bf16(np.ascontiguousarray(cidx, dtype=np.float32))
+    q_idx = S.round_bf16(rng.standard_normal((B, 1, H_idx, 128), dtype=np.float32) / np.float32(np.sqrt(128)))
+    w = (np.abs(rng.standard_normal((B, 1, H_idx))) / np.sqrt(128 * H_idx)).astype(np.float32)
+    c = L.Config(top_k=k, ratio=4)
+    pos = np.array([[4 * n_cap - 1], [4 * (n_cap - 1000) - 3]], np.int64)
+    topk = torch.empty(B, 1, k, dtype=torch.int32, device="cuda")
+    scores = torch.full((B, 1, n_cap), float("nan"), device="cuda")
+    L.csa_index_topk(c, torch.from_numpy(pos).cuda(), Hn.dev(q_idx, "bf16"), torch.from_numpy(w).cuda(),
+                     Hn.dev(cidx, "bf16"), topk, scores)
+    torch.cuda.synchronize()
+    for b in range(B):
+        V = O.visible(int(pos[b, 0]), 4)
+        got = scores[b, 0, :V].double().cpu().numpy()
+        Hn.check_topk_exact(topk[b, 0].cpu().numpy(), got, k, f"{mode} b{b}")
+    assert L.csa_get_device_status() == 0
