@@ -34,6 +34,26 @@ DECODE_WL = synth.WORKLOADS[1]
 PREFILL_WL = synth.WORKLOADS[2]
 ROTATIONS = 3                      # input copies cycled between steps (defeats the 126 MB L2)
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+# DRAM bytes (read + write) of one decode indexer launch at the decode workload, from an ncu capture
+# (profiles/index_tc_decode_B32_N65536.md). They hold only for the kernel source they were taken
+# on: the roofline's "traffic" is null as soon as any of these files differs from that capture.
+INDEX_TRAFFIC = {"bytes_per_launch": 134789632 + 552576,
+                 "sources": ["long_context_sparse_19_b300/csrc/tc_index.cu",
+                             "long_context_sparse_19_b300/csrc/tc_ptx.cuh",
+                             "long_context_sparse_19_b300/csrc/common.cuh"],
+                 "sha256": "6301b16e7048dcaacf9f9c1e224e34454fb06900414c0c0af1ddffc112f4c80d"}
+# GPU sleep queued ahead of each profiled step, so that the host has submitted the whole step before
+# it starts and the per-kernel events time the GPU, not the host's launch rate (~250 us at 2 GHz)
+PROFILE_SLEEP_CYCLES = 500_000
+
+
+def index_traffic() -> int | None:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in INDEX_TRAFFIC["sources"]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return INDEX_TRAFFIC["bytes_per_launch"] if h.hexdigest() == INDEX_TRAFFIC["sha256"] else None
 
 
 def load_peaks() -> dict:
@@ -283,16 +303,14 @@ def run_decode(args, world, rank, device, peaks) -> dict:
     clk = clocks.summary(wall0, wall1)
 
     # Second pass, same steps without the graph, with a CUDA event pair around every kernel on its
-    # launching stream: per-kernel average durations for the roofline.
+    # launching stream: per-kernel average durations for the roofline. A GPU sleep ahead of each
+    # step lets the host queue the whole step first, so no event waits on a host-side launch.
     L.csa_profile_begin(K * launches_per_step + 16)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
     for i in range(K):
+        torch.cuda._sleep(PROFILE_SLEEP_CYCLES)
         rot[i % R]["call"]()
-    e1.record()
     torch.cuda.synchronize()
     prof = L.csa_profile_end()
-    eager_ms = e0.elapsed_time(e1)
 
     # End to end: per step, the step's inputs (q, q_idx, w, the new token's raw rows) come from
     # pinned host memory and the output goes back to pinned host memory, all inside the region.
@@ -309,12 +327,13 @@ def run_decode(args, world, rank, device, peaks) -> dict:
         "value": qtok, "ms_per_step": ms_max / K, "hbm_gbs": work["bytes"] / step_s / 1e9,
         "hbm_frac_of_measured": work["bytes"] / step_s / 1e9 / peaks["hbm_gbs"],
         "step_bytes": work["bytes"], "step_flops": work["flops"], "gpu_launches": launches_per_step * K,
-        "clocks": clk, "setup_s": round(setup_s, 1), "eager_ms_per_step": eager_ms / K,
+        "clocks": clk, "setup_s": round(setup_s, 1),
+        "stage_sum_ms_per_step": sum(v[0] for v in prof.values()) / K,
         "stages_ms_per_step": {k: round(v[0] / K, 5) for k, v in prof.items()},
         "stage_launches": {k: v[1] for k, v in prof.items()},
         "roofline": {"kernel": "indexer scores (csa_index_topk / csa_decode stage 1)", "bound": "hbm",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": (achieved / peaks["hbm_gbs"]) if achieved else None, "traffic": None,
+                     "frac": (achieved / peaks["hbm_gbs"]) if achieved else None, "traffic": index_traffic(),
                      "algorithmic_bytes_per_launch": work["index_bytes"],
                      "avg_launch_us": idx_avg_s * 1e6, "peak_source": peaks["source"]},
         "e2e": e2e,
@@ -566,7 +585,7 @@ def main():
                 "hbm_gbs": dec["hbm_gbs"], "hbm_frac_of_measured": dec["hbm_frac_of_measured"],
                 "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
                 "gpu_launches": dec["gpu_launches"], "clocks": dec["clocks"],
-                "detail": {k: dec[k] for k in ("step_bytes", "step_flops", "eager_ms_per_step",
+                "detail": {k: dec[k] for k in ("step_bytes", "step_flops", "stage_sum_ms_per_step",
                                                "stages_ms_per_step", "stage_launches", "setup_s")},
                 "prefill": pre}
         print(json.dumps(line), flush=True)

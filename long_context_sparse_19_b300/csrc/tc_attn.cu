@@ -12,8 +12,8 @@
 // One CTA = one query and one or two 128-candidate tiles (window tiles first, then compressed
 // tiles). Decode batches use one tile per CTA: the grid lists every query's window tile first and
 // those CTAs never wait for the selection kernel, so under programmatic dependent launch they run
-// while the selection is still being computed; the compressed tiles follow in one wave, their
-// rows already requested into L2 by the selection kernel. A tile streams through a 4-stage ring in
+// while the selection is still being computed; the compressed tiles follow, and every CTA asks L2
+// for all of its rows at once before its first gather. A tile streams through a 4-stage ring in
 // 32 KB K-chunks (128 candidates x 128 dims); with two tiles per CTA the last tile of the S^T phase
 // stays resident for the O^T phase and only the other one is gathered again (an L2 hit).
 // Warps:
