@@ -239,8 +239,8 @@ csa_status check_ws(const Plan& pl, void* ws, size_t ws_bytes) {
 }
 
 // ------------------------------------------------------------------ stage launchers
-csa_status run_compress(const csa_config* c, int B, const csa_cache* k, int64_t first, int64_t n,
-                        const int64_t* pos, cudaStream_t st) {
+CompressParams compress_params(const csa_config* c, const csa_cache* k, int64_t first, int64_t n,
+                               const int64_t* pos) {
   CompressParams p;
   memset(&p, 0, sizeof p);
   p.job[0] = CompressJob{k->kv, k->gate, k->gate_bias, k->ckv, c->d};
@@ -251,6 +251,12 @@ csa_status run_compress(const csa_config* c, int B, const csa_cache* k, int64_t 
   }
   p.N = k->N; p.n_cap = k->n_cap; p.first_entry = first; p.n_entries = n; p.pos = pos;
   p.ratio = c->ratio; p.eps = c->rms_eps; p.rope = make_rope(c); p.err = device_error_word();
+  return p;
+}
+
+csa_status run_compress(const csa_config* c, int B, const csa_cache* k, int64_t first, int64_t n,
+                        const int64_t* pos, cudaStream_t st) {
+  const CompressParams p = compress_params(c, k, first, n, pos);
   // the compressor is the first kernel of every call that runs it: a normal (fully ordered) launch
   return cuda_status(
       launch_stage(ST_COMPRESS, st, [&] { return launch_compress(c->storage == CSA_BF16, B, p, st, false); }),
@@ -259,13 +265,14 @@ csa_status run_compress(const csa_config* c, int B, const csa_cache* k, int64_t 
 
 csa_status run_index_topk(const csa_config* c, int B, int S, const int64_t* pos, const void* q_idx,
                           const float* w, const void* cidx, int64_t n_cap, int32_t* topk,
-                          float* scores, void* tk_ws, void* tc_ws, cudaStream_t st, bool pdl) {
+                          float* scores, void* tk_ws, void* tc_ws, cudaStream_t st, bool pdl,
+                          const CompressParams* close = nullptr) {
   const bool bf16 = c->storage == CSA_BF16;
   if (use_tc_index(c)) {
     const RopeTab rope = make_rope(c);
     int32_t* err = device_error_word();
     cudaError_t e = launch_stage(ST_INDEX, st, [&] {
-      return tc_index_scores(B, S, pos, q_idx, w, cidx, n_cap, c->ratio, rope, scores, tc_ws, err, st, pdl);
+      return tc_index_scores(B, S, pos, q_idx, w, cidx, n_cap, c->ratio, rope, scores, tc_ws, err, st, pdl, close);
     });
     if (e != cudaSuccess) return cuda_status(e, "tcgen05 indexer launch");
   } else {
@@ -451,14 +458,21 @@ csa_status csa_decode(const csa_config* cfg, int32_t B, const int64_t* pos, cons
   s = check_ws(pl, ws, ws_bytes);
   if (s != CSA_OK) return s;
   if (B == 0) return CSA_OK;
-  s = run_compress(cfg, B, cache, 0, 0, pos, stream);
-  if (s != CSA_OK) return s;
+  // CSA with the tensor-core indexer: the step's first kernel is the indexer, which also pools the
+  // entries that t closes (both caches) before the scores need them. Otherwise the compressor's
+  // close kernel runs first.
+  const bool fused_close = !hca && use_tc_index(cfg);
+  const CompressParams close = compress_params(cfg, cache, 0, 0, pos);
+  if (!fused_close) {
+    s = run_compress(cfg, B, cache, 0, 0, pos, stream);
+    if (s != CSA_OK) return s;
+  }
   int32_t* tk = nullptr;
   if (!hca) {
     tk = topk_out ? topk_out : carve<int32_t>(ws, pl.off_topk);
     s = run_index_topk(cfg, B, 1, pos, q_idx, w, cache->cidx, cache->n_cap, tk,
                        carve<float>(ws, pl.off_scores), carve<char>(ws, pl.off_tksel), carve<char>(ws, pl.off_tc),
-                       stream, true);
+                       stream, !fused_close, fused_close ? &close : nullptr);
     if (s != CSA_OK) return s;
   }
   return run_attn(cfg, pl, B, 1, pos, q, cache->kv, cache->N, cache->ckv, cache->n_cap, tk, sink, out, ws,

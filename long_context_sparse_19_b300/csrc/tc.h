@@ -19,9 +19,13 @@ int tc_sm_count();
 cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, int64_t rows, uint32_t cols, uint32_t box_rows);
 
 // s_i = sum_h w_h relu(rope(q_h, t) . cidx_i) for i < visible(t), bf16 operands, fp32 accumulate.
+// `close` (decode, S = 1; null otherwise): the compressor's close step for both caches (job[0] the
+// 512-channel KV cache, job[1] the index cache) runs inside this kernel, before the scores that
+// need it; the kernel is then the step's first and must not be a dependent launch.
 cudaError_t tc_index_scores(int B, int S, const int64_t* pos, const void* q_idx, const float* w,
                             const void* cidx, int64_t n_cap, int ratio, const RopeTab& rope,
-                            float* scores, void* ws, int32_t* err, cudaStream_t st, bool pdl);
+                            float* scores, void* ws, int32_t* err, cudaStream_t st, bool pdl,
+                            const CompressParams* close = nullptr);
 
 // Many-query attention (prefill): one CTA per query over all of its candidates (at most
 // tc_attn_prefill_max_tiles() tiles of 128), final output written directly.

@@ -20,6 +20,7 @@
 
 #include <mutex>
 
+#include "close_entry.cuh"
 #include "tc.h"
 #include "tc_ptx.cuh"
 
@@ -47,6 +48,9 @@ struct IndexTcParams {
   int S, ratio, chunks;
   RopeTab rope;
   int32_t* err;
+  // decode only (close.job[0].src non-null): the entry that t closes is pooled here first, the
+  // index entry by the CTA that scores it and the KV entry by the CTA that owns tile 0
+  CompressParams close;
 };
 
 __global__ void __launch_bounds__(kThreads, 2)
@@ -61,8 +65,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* tfull = bars + 2 * kStages;                     // [2]
   uint64_t* tempty = bars + 2 * kStages + 2;                // [2]
   uint64_t* qready = bars + 2 * kStages + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  uint64_t* closed = bars + 2 * kStages + 5;                // the index entry is in global memory
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 6);
   float* w_s = reinterpret_cast<float*>(tmem_slot + 4);    // [64]
+  float* red = w_s + 64;                                    // [2][4]
 
   if (threadIdx.x == 0) CSA_STAMP(42);
   griddep_launch();
@@ -72,15 +78,28 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int64_t t = p.pos ? p.pos[row] : s;
   const int64_t V = t < 0 ? 0 : min(visible_entries(t, p.ratio), p.n_cap);
   const int64_t T = (V + kTileM - 1) / kTileM;
-  const int64_t tile0 = (int64_t)blockIdx.x * T / p.chunks;
-  const int64_t tile1 = (int64_t)(blockIdx.x + 1) * T / p.chunks;
+  // decode close: t completes group e = t / m, which makes entry e = V - 1 visible (uniform per CTA)
+  const bool fused = p.close.job[0].src != nullptr;
+  const bool group_done = fused && t >= 0 && t < p.close.N && (t + 1) % p.ratio == 0;
+  if (fused && blockIdx.x == 0 && threadIdx.x == 0 && (t < 0 || t >= p.close.N || (group_done && t / p.ratio >= p.n_cap)))
+    set_error(p.err, DEVERR_BAD_POS);
+  const bool closes = group_done && t / p.ratio < p.n_cap;  // then V = e + 1: entry e is the last visible
+  // pooling the KV entry costs the tile-0 CTA about one tile: with a close, that CTA gets one
+  // tile fewer (the split runs over T + 1 tiles, the first of them virtual)
+  const int64_t Tv = closes && p.chunks > 1 ? T + 1 : T;
+  const int64_t sh = Tv - T;
+  const int64_t tile0 = max((int64_t)blockIdx.x * Tv / p.chunks - sh, (int64_t)0);
+  const int64_t tile1 = max((int64_t)(blockIdx.x + 1) * Tv / p.chunks - sh, (int64_t)0);
   const int ntiles = (int)(tile1 - tile0);
   if (ntiles <= 0) return;                                  // uniform over the CTA
+  const bool close_kv = closes && tile0 == 0;               // pools ckv entry e
+  const bool close_idx = closes && tile1 == T;              // pools cidx entry e, scored in its last tile
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&tfull[i], 1); mbar_init(&tempty[i], 128); }
     mbar_init(qready, 128);
+    mbar_init(closed, 128);
     fence_mbar_init();
   }
   if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
@@ -99,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages;
         if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1, p.err)) break;
+        if (close_idx && i == ntiles - 1 && !mbar_wait(closed, 0, p.err)) break;   // holds entry e
         mbar_arrive_expect_tx(&full[st], kTileBytes);
         const int32_t y = (int32_t)(b * p.n_cap + (tile0 + i) * kTileM);
         uint8_t* dst = stage_base + st * kTileBytes;
@@ -170,6 +190,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     fence_proxy_async_smem();
     mbar_arrive(qready);
     named_barrier(1, 128);                                  // w_s visible to every epilogue thread
+    const int64_t e = t / p.ratio;
+    if (close_kv)
+      close_entry_bf16<512>(p.close.job[0], p.close.N, p.n_cap, p.ratio, p.close.eps, p.close.rope, b, e, et,
+                            red, 2);
+    if (close_idx) {
+      close_entry_bf16<128>(p.close.job[1], p.close.N, p.n_cap, p.ratio, p.close.eps, p.close.rope, b, e, et,
+                            red + 4, 2);
+      fence_proxy_async_global();                           // the TMA load of the last tile reads it
+      mbar_arrive(closed);
+    }
 
     const uint32_t quad = warp & 3;                         // TMEM lanes 32*quad .. 32*quad+31
     float* out = p.scores + row * p.n_cap;
@@ -249,7 +279,7 @@ int tc_sm_count() {
 
 cudaError_t tc_index_scores(int B, int S, const int64_t* pos, const void* q_idx, const float* w, const void* cidx,
                             int64_t n_cap, int ratio, const RopeTab& rope, float* scores, void*, int32_t* err,
-                            cudaStream_t st, bool pdl) {
+                            cudaStream_t st, bool pdl, const CompressParams* close) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(index_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
@@ -262,6 +292,11 @@ cudaError_t tc_index_scores(int B, int S, const int64_t* pos, const void* q_idx,
   IndexTcParams p;
   p.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
   p.w = w; p.scores = scores; p.pos = pos; p.n_cap = n_cap; p.S = S; p.ratio = ratio; p.rope = rope; p.err = err;
+  memset(&p.close, 0, sizeof p.close);
+  if (close) {
+    if (S != 1 || close->n_jobs != 2 || close->job[0].C != 512 || close->job[1].C != kDI) return cudaErrorInvalidValue;
+    p.close = *close;
+  }
   const int64_t tiles = (n_cap + kTileM - 1) / kTileM;
   const int64_t rows = (int64_t)B * S;
   int64_t chunks = (2 * (int64_t)tc_sm_count()) / (rows > 0 ? rows : 1);   // two CTAs per SM, one wave

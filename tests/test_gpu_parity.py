@@ -26,6 +26,9 @@ DECODE = {
     # more tiles than two waves of CTAs: two tiles per CTA, one of them gathered twice
     "csa_bf16_B64": (synth.small_workload(1, wid=106, B=64, N=2051, t=2050),
                      [2050 - 13 * b for b in range(64)]),
+    # the first groups: entry 0 closes at t = 3 (its previous group lies before position 0, weight
+    # 0), entry 1 at t = 7; t = 0 and t = 2 see no compressed entry at all
+    "csa_bf16_early": (synth.small_workload(1, wid=107, B=5, N=520, t=519), [3, 7, 2, 0, 519]),
 }
 MODES = [False, True]          # tensor-core path where available, then the CUDA-core path
 
