@@ -166,6 +166,10 @@ __device__ __forceinline__ void dsmem_add(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void dsmem_st(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+__device__ __forceinline__ void dsmem_st4(uint32_t addr, uint4 v) {   // addr 16-byte aligned
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w) : "memory");
+}
 
 // ------------------------------------------------------------------ phase stamps
 // CSA_STAMP(slot) records %globaltimer for (CTA, slot) in a device table when the library is

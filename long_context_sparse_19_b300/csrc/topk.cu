@@ -270,33 +270,35 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const SelParams p
 // A row of up to 8 x 2048 items is selected by one thread-block cluster in a single launch. CTA r
 // of the cluster holds items 2048 r .. 2048 r + 2047 (16 per thread, in registers). The CTAs share
 // what they find by writing into each other's shared memory (remote adds and stores: no round
-// trips) followed by a cluster barrier. Remote requests are slow one by one, so each CTA sends as
-// few as it can:
+// trips) followed by a cluster barrier. A remote request costs a few hundred nanoseconds and one
+// thread's requests do not overlap, so each CTA sends as few as it can:
 //   1. every CTA adds its histogram of the keys' top 11 bits into every CTA's copy of the cluster
-//      histogram, but only from the bin of its own k-th largest key upwards: the row's k-th largest
-//      key is at least as large, so the bins below cannot hold it. After the barrier each CTA finds
-//      the same threshold bin (a bin of more than kListCap items is first refined by the next 11
-//      bits through another exchange);
-//   2. every CTA stores its counts of items above the bin and in it into every CTA, and, when the
-//      bin must be split, its in-bin keys in index order; after the barrier every CTA holds the
-//      bin's keys in row order and finds the last digits of the threshold on its own;
-// then every CTA writes its winners in ascending index order. No CTA writes to another after the
-// last barrier it takes part in, so none can exit while another still writes to it. Shared memory
-// is kept near 40 KB: a larger footprint delays placing the 8-CTA clusters beside the indexer and
-// attention CTAs of neighbouring launches, which costs more than the rarer second exchange saves.
+//      histogram, and into a second array of the higher-ranked CTAs only, but only from the bin
+//      of its own k-th largest key upwards (the row's k-th largest key is at least as large, so
+//      lower bins cannot hold it). After the barrier each CTA finds the same threshold bin, and
+//      the second array tells it how many items above the bin and in it the lower-ranked CTAs
+//      hold: where its own winners go in the output;
+//   2. when only part of the bin is taken, every CTA stores its in-bin keys into every CTA's list
+//      at those offsets (row order); after the barrier each finds the remaining digits of the
+//      threshold on its own and takes the first `need` in-bin keys in (-key, position) order;
+// then every CTA writes its winners in ascending index order. A bin of more than kListCap items
+// (a very flat distribution) is first refined by the next digits through further exchanges, with
+// the offsets then exchanged as counts. No CTA writes to another after the last barrier it takes
+// part in, so none can exit while another still writes to it. Shared memory is kept near 45 KB: a
+// larger footprint delays placing the 8-CTA clusters beside the CTAs of neighbouring launches.
 constexpr int kCluThreads = 128;
 constexpr int kCluChunk = kCluThreads * kItems;          // 2048 items per CTA
 constexpr int kCluMax = 8;                                // portable cluster size
-constexpr int kListCap = 256;                             // in-bin items split locally (cluster total)
+constexpr int kListCap = 1024;                            // in-bin items split locally (cluster total)
 constexpr int kListPer = kListCap / kCluThreads;          // list positions per thread in the final order
 static_assert(kListCap % kCluThreads == 0, "the final order gives each thread the same number of list positions");
 
 struct CluSmem {
   uint32_t full[3][kBins];              // cluster histogram of each digit pass (remote adds)
+  uint32_t before[kBins];               // first digit, lower-ranked CTAs only (remote adds)
   uint32_t hist[kBins];                 // this CTA's histogram; later the local digit passes
-  uint32_t list[kCluMax][kListCap];     // in-bin keys of each source CTA, index order (remote stores)
-  uint32_t all_list[kListCap];          // the same, concatenated in row order
-  uint32_t src_cnt[kCluMax][2];         // per source CTA: (items above the bin, in it) (remote stores)
+  alignas(16) uint32_t list[kListCap];  // the cluster's in-bin keys in row order (remote stores)
+  uint32_t src_cnt[kCluMax][2];         // per source CTA: (items above, in the class) (remote stores)
   uint32_t n_valid;                     // the row's valid items (remote adds)
   uint32_t scr[64];
   uint32_t res[4];
@@ -309,7 +311,7 @@ __global__ void __launch_bounds__(kCluThreads) topk_cluster_kernel(const SelPara
   if (threadIdx.x == 0) CSA_STAMP(47);
   const int tid = threadIdx.x, lane = tid & 31;
   const uint32_t rank = cluster_rank(), C = gridDim.x;
-  for (int i = tid; i < 3 * kBins; i += kCluThreads) (&sm.full[0][0])[i] = 0;
+  for (int i = tid; i < 4 * kBins; i += kCluThreads) (&sm.full[0][0])[i] = 0;   // full and before
   if (tid == 0) sm.n_valid = 0;
   cluster_arrive();                                       // the zeroed counters may be added into
   griddep_launch();
@@ -387,8 +389,11 @@ __global__ void __launch_bounds__(kCluThreads) topk_cluster_kernel(const SelPara
     }
     for (int i = tid; i < kBins; i += kCluThreads) {
       const uint32_t v = sm.hist[i];
-      if (v != 0u && (uint32_t)i >= floor_bin)
+      if (v != 0u && (uint32_t)i >= floor_bin) {
         for (uint32_t r = 0; r < C; ++r) dsmem_add(dsmem_addr(&sm.full[pass][i], r), v);
+        if (pass == 0)
+          for (uint32_t r = rank + 1; r < C; ++r) dsmem_add(dsmem_addr(&sm.before[i], r), v);
+      }
     }
     cluster_sync();                                       // every CTA's additions have landed
     if (tid == 0) CSA_STAMP(pass == 0 ? 57 : 53);
@@ -422,36 +427,57 @@ __global__ void __launch_bounds__(kCluThreads) topk_cluster_kernel(const SelPara
   block_scan2<kCluThreads>(ngt, neq, sm.scr, rg, re, GT, EQ);
   // the class is split locally when only part of it is taken and digits remain (the same in every CTA)
   const bool split = !take_all && class_cnt > need && pmask != 0xFFFFFFFFu;
-  if (tid < (int)C) {
-    const uint32_t at = dsmem_addr(&sm.src_cnt[rank][0], (uint32_t)tid);
-    dsmem_st(at, GT);
-    dsmem_st(at + 4, EQ);
-  }
-  if (split) {                                            // class_cnt <= kListCap here
-    uint32_t e = re;
+  uint32_t gt_off = 0, eq_off = 0, eq_total = take_all ? 0u : class_cnt;
+  if (pass == 0) {
+    // resolved by the first digit: the lower-ranked CTAs' counts are in `before` (every bin above
+    // the threshold bin, or every bin when all is taken, was sent by every CTA)
+    const uint32_t bstar = prefix >> 21;
+    uint32_t above = 0;
 #pragma unroll
-    for (int u = 0; u < kItems; ++u)
-      if (key[u] != 0u && (key[u] & pmask) == prefix) {
-        for (uint32_t r = 0; r < C; ++r) dsmem_st(dsmem_addr(&sm.list[rank][e], r), key[u]);
-        ++e;
-      }
+    for (int u = 0; u < kItems; ++u) {
+      const uint32_t bin = kBins - 1 - kItems * tid - u;
+      if (take_all || bin > bstar) above += sm.before[bin];
+    }
+    uint32_t d0, d1, d2;
+    block_scan2<kCluThreads>(above, 0u, sm.scr, d0, d1, gt_off, d2);
+    eq_off = take_all ? 0u : sm.before[bstar];
+  } else {
+    // refined by further digits: exchange the counts
+    if (tid < (int)C) {
+      const uint32_t at = dsmem_addr(&sm.src_cnt[rank][0], (uint32_t)tid);
+      dsmem_st(at, GT);
+      dsmem_st(at + 4, EQ);
+    }
+    cluster_sync();                                       // every CTA's counts have landed
+    for (uint32_t r = 0; r < rank; ++r) { gt_off += sm.src_cnt[r][0]; eq_off += sm.src_cnt[r][1]; }
   }
   if (tid == 0) CSA_STAMP(61);
-  cluster_sync();                                         // counts and lists have landed: the last barrier
-  uint32_t gt_off = 0, eq_off = 0, eq_total = 0;
-  for (uint32_t r = 0; r < C; ++r) {
-    if (r < rank) { gt_off += sm.src_cnt[r][0]; eq_off += sm.src_cnt[r][1]; }
-    eq_total += sm.src_cnt[r][1];
-  }
   const bool all_eq_taken = take_all || eq_total <= need;
   const bool by_position = !all_eq_taken && !split;       // all 32 bits fixed: equal keys, first `need`
-  if (split) {
-    for (uint32_t gpos = tid; gpos < eq_total; gpos += kCluThreads) {
-      uint32_t r = 0, base = 0;
-      while (r + 1 < C && gpos >= base + sm.src_cnt[r][1]) { base += sm.src_cnt[r][1]; ++r; }
-      sm.all_list[gpos] = sm.list[r][gpos - base];
-    }
+  if (split) {                                            // eq_total <= kListCap here
+    // this CTA's in-bin keys go to their row-order positions [eq_off, eq_off + EQ) of the local
+    // list first, then to every other CTA, spread evenly over the threads: 16-byte stores for the
+    // aligned middle of the segment, single words at its two ends
+    uint32_t e = eq_off + re;
+#pragma unroll
+    for (int u = 0; u < kItems; ++u)
+      if (key[u] != 0u && (key[u] & pmask) == prefix) sm.list[e++] = key[u];
     __syncthreads();
+    const uint32_t lo = eq_off, hi = eq_off + EQ;
+    const uint32_t qlo = min((lo + 3u) & ~3u, hi), qhi = max(hi & ~3u, qlo);
+    const uint32_t nq = (qhi - qlo) / 4, n_lo = qlo - lo, items = nq + n_lo + (hi - qhi);
+    for (uint32_t w = tid; w < items * (C - 1); w += kCluThreads) {
+      const uint32_t item = w / (C - 1), d = w % (C - 1), r = d < rank ? d : d + 1;
+      if (item < nq) {
+        const uint32_t at = qlo + 4 * item;
+        dsmem_st4(dsmem_addr(&sm.list[at], r), *reinterpret_cast<const uint4*>(&sm.list[at]));
+      } else {
+        const uint32_t j = item - nq, at = j < n_lo ? lo + j : qhi + (j - n_lo);
+        dsmem_st(dsmem_addr(&sm.list[at], r), sm.list[at]);
+      }
+    }
+    cluster_sync();                                       // the list is complete: the last barrier
+    if (tid == 0) CSA_STAMP(49);
     // the remaining digits of the threshold, over the class's keys only
     uint32_t lp = prefix, lm = pmask, ln = need;
     for (int dp = pass + 1; dp < 3; ++dp) {
@@ -460,7 +486,7 @@ __global__ void __launch_bounds__(kCluThreads) topk_cluster_kernel(const SelPara
       for (int i = tid; i < kBins; i += kCluThreads) sm.hist[i] = 0;
       __syncthreads();
       for (uint32_t gpos = tid; gpos < eq_total; gpos += kCluThreads) {
-        const uint32_t kv = sm.all_list[gpos];
+        const uint32_t kv = sm.list[gpos];
         if ((kv & lm) == lp) atomicAdd(&sm.hist[(kv >> shift) & dmask], 1u);
       }
       __syncthreads();
@@ -477,13 +503,13 @@ __global__ void __launch_bounds__(kCluThreads) topk_cluster_kernel(const SelPara
     uint32_t c = 0;
 #pragma unroll
     for (int j = 0; j < kListPer; ++j)
-      c += q0 + j < eq_total && (sm.all_list[q0 + j] & lm) == lp;
+      c += q0 + j < eq_total && (sm.list[q0 + j] & lm) == lp;
     uint32_t ce, d0, d1, d2;
     block_scan2<kCluThreads>(c, 0u, sm.scr, ce, d0, d1, d2);
 #pragma unroll
     for (int j = 0; j < kListPer; ++j)
       if (q0 + j < eq_total) {
-        const uint32_t m = sm.all_list[q0 + j] & lm;
+        const uint32_t m = sm.list[q0 + j] & lm;
         sm.taken[q0 + j] = m > lp || (m == lp && ce++ < ln);
       }
     __syncthreads();
