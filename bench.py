@@ -37,11 +37,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one decode indexer launch at the decode workload, from an ncu capture
 # (profiles/index_tc_decode_B32_N65536.md). They hold only for the kernel source they were taken
 # on: the roofline's "traffic" is null as soon as any of these files differs from that capture.
-INDEX_TRAFFIC = {"bytes_per_launch": 134789632 + 552576,
+INDEX_TRAFFIC = {"bytes_per_launch": 135505920 + 1793024,
                  "sources": ["long_context_sparse_19_b300/csrc/tc_index.cu",
                              "long_context_sparse_19_b300/csrc/tc_ptx.cuh",
-                             "long_context_sparse_19_b300/csrc/common.cuh"],
-                 "sha256": "6301b16e7048dcaacf9f9c1e224e34454fb06900414c0c0af1ddffc112f4c80d"}
+                             "long_context_sparse_19_b300/csrc/common.cuh",
+                             "long_context_sparse_19_b300/csrc/close_entry.cuh"],
+                 "sha256": "d8801a5686fc862504b08eccbcbfdf046dab4d7957fa6128568926819d96464b"}
 # GPU sleep queued ahead of each profiled step, so that the host has submitted the whole step before
 # it starts and the per-kernel events time the GPU, not the host's launch rate (~250 us at 2 GHz)
 PROFILE_SLEEP_CYCLES = 500_000
@@ -262,7 +263,8 @@ def run_decode(args, world, rank, device, peaks) -> dict:
             q, qi, w = rot[0]["q"].clone(), rot[0]["q_idx"].clone(), rot[0]["w"].clone()
         out = torch.empty(B, wl.H, wl.d, dtype=cache.kv.dtype, device=device)
         ws = L.workspace(cfg, B, 1, wl.n_entries, device=device)
-        rot.append({"cache": c, "q": q, "q_idx": qi, "w": w, "out": out, "pos": pos.clone(), "ws": ws})
+        rot.append({"cache": c, "q": q, "q_idx": qi, "w": w, "out": out, "pos": pos.clone(), "ws": ws, "cfg": cfg,
+                    "sink": T["sink"]})
         rot[-1]["call"] = L.binding.bind_decode(cfg, rot[-1]["pos"], c, q, qi, w, T["sink"], out, ws=ws)
     torch.cuda.synchronize()
     setup_s = time.time() - t_setup
@@ -352,49 +354,73 @@ def gpu_ident(device) -> str:
 
 def run_e2e(args, wl, rot, world, device) -> dict:
     import torch
+    import long_context_sparse_19_b300 as L
     B, t = wl.B, wl.t
     dt = rot[0]["q"].dtype
-    host = []
+    # Per input copy: the step's inputs packed in one pinned host buffer (q, q_idx, w, pos and the
+    # new token's raw rows of the four raw caches), uploaded by one copy into a device staging
+    # buffer; csa_decode reads q, q_idx, w and pos in place there, and the raw rows are copied into
+    # the caches on the device.
+    parts = [("q", (B, wl.H, wl.d), dt), ("q_idx", (B, wl.H_idx, wl.d_idx), dt), ("w", (B, wl.H_idx), torch.float32),
+             ("pos", (B,), torch.int64), ("kv", (B, wl.d), dt), ("gate", (B, wl.d), dt),
+             ("idx_k", (B, wl.d_idx), dt), ("idx_gate", (B, wl.d_idx), dt)]
+    offs, o = {}, 0
+    for name, shape, typ in parts:
+        offs[name] = o
+        o += -(-math.prod(shape) * torch.empty((), dtype=typ).element_size() // 256) * 256
+    total = o
+
+    def views(buf):
+        out = {}
+        for name, shape, typ in parts:
+            n = math.prod(shape) * torch.empty((), dtype=typ).element_size()
+            out[name] = buf[offs[name]:offs[name] + n].view(typ).view(shape)
+        return out
+
+    host, stage = [], []
     for r in rot:
         c = r["cache"]
-        hb = {"q": r["q"].cpu().pin_memory(), "q_idx": r["q_idx"].cpu().pin_memory(),
-              "w": r["w"].cpu().pin_memory(), "pos": r["pos"].cpu().pin_memory(),
-              "kv": c.kv[:, t].cpu().pin_memory(), "gate": c.gate[:, t].cpu().pin_memory(),
-              "idx_k": c.idx_k[:, t].cpu().pin_memory(), "idx_gate": c.idx_gate[:, t].cpu().pin_memory(),
-              "out": torch.empty((B, wl.H, wl.d), dtype=dt).pin_memory()}
-        host.append(hb)
-    h2d = sum(host[0][k].numel() * host[0][k].element_size()
-              for k in ("q", "q_idx", "w", "pos", "kv", "gate", "idx_k", "idx_gate"))
+        hbuf = torch.empty(total, dtype=torch.uint8).pin_memory()
+        hv = views(hbuf)
+        src = {"q": r["q"], "q_idx": r["q_idx"], "w": r["w"], "pos": r["pos"], "kv": c.kv[:, t], "gate": c.gate[:, t],
+               "idx_k": c.idx_k[:, t], "idx_gate": c.idx_gate[:, t]}
+        for name in hv:
+            hv[name].copy_(src[name].cpu())
+        dbuf = torch.empty(total, dtype=torch.uint8, device=device)
+        dv = views(dbuf)
+        stage.append({"buf": dbuf, **dv})
+        host.append({"buf": hbuf, "out": torch.empty((B, wl.H, wl.d), dtype=dt).pin_memory()})
+        # the decode call reads its per-step inputs straight from the staging buffer
+        r["e2e_call"] = L.binding.bind_decode(r["cfg"], dv["pos"], c, dv["q"], dv["q_idx"], dv["w"], r["sink"],
+                                              r["out"], ws=r["ws"])
+    h2d = total
     d2h = host[0]["out"].numel() * host[0]["out"].element_size()
 
     R = len(rot)
 
-    def upload(r, hb):
+    def upload(r, hb, sb):
         c = r["cache"]
-        r["q"].copy_(hb["q"], non_blocking=True)
-        r["q_idx"].copy_(hb["q_idx"], non_blocking=True)
-        r["w"].copy_(hb["w"], non_blocking=True)
-        r["pos"].copy_(hb["pos"], non_blocking=True)
-        c.kv[:, t].copy_(hb["kv"], non_blocking=True)
-        c.gate[:, t].copy_(hb["gate"], non_blocking=True)
-        c.idx_k[:, t].copy_(hb["idx_k"], non_blocking=True)
-        c.idx_gate[:, t].copy_(hb["idx_gate"], non_blocking=True)
+        sb["buf"].copy_(hb["buf"], non_blocking=True)
+        c.kv[:, t].copy_(sb["kv"])
+        c.gate[:, t].copy_(sb["gate"])
+        c.idx_k[:, t].copy_(sb["idx_k"])
+        c.idx_gate[:, t].copy_(sb["idx_gate"])
 
     # How a serving loop runs the step: per input copy, one CUDA graph uploads the step's inputs
     # from pinned host memory, one runs csa_decode, one reads the output back to pinned host
     # memory, on three streams, so that step i+1's upload and step i-1's read-back overlap step i.
     s_up, s_run, s_down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     g_up, g_run, g_down = [], [], []
-    for r, hb in zip(rot, host):
-        upload(r, hb)
-        r["call"]()
+    for r, hb, sb in zip(rot, host, stage):
+        upload(r, hb, sb)
+        r["e2e_call"]()
         hb["out"].copy_(r["out"], non_blocking=True)
         torch.cuda.synchronize()
         gu, gr, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.graph(gu, stream=s_up):
-            upload(r, hb)
+            upload(r, hb, sb)
         with torch.cuda.graph(gr, stream=s_run):
-            r["call"]()
+            r["e2e_call"]()
         with torch.cuda.graph(gd, stream=s_down):
             hb["out"].copy_(r["out"], non_blocking=True)
         g_up.append(gu); g_run.append(gr); g_down.append(gd)
@@ -434,8 +460,9 @@ def run_e2e(args, wl, rot, world, device) -> dict:
     el = max_over_ranks(el, world)
     return {"value": world * B * K / el, "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": el / K * 1e3,
-            "how": "per step: upload graph (pinned host -> device), csa_decode graph, read-back graph "
-                   "(device -> pinned host) on three streams; consecutive steps overlap; wall clock"}
+            "how": "per step: one packed upload from pinned host memory (+ the raw rows placed into the "
+                   "caches on the device), csa_decode, read-back to pinned host memory; one CUDA graph "
+                   "each on three streams, consecutive steps overlap; wall clock"}
 
 
 # ----------------------------------------------------------------------------- prefill leg
