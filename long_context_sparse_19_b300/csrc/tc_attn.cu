@@ -25,7 +25,9 @@
 //        TMEM: per-head max and sum by a butterfly reduce-scatter across lanes plus a 4-warp
 //        combine, P^T (bf16) into shared memory, and finally write the split partial (max, sum, O);
 //   6    rotates the query at t (RoPE on dims 448..511) in shared memory. Raw window rows are
-//        rotated at their own positions by the gather threads, each in the pieces it copied.
+//        rotated at their own positions by the gather threads, each in the pieces it copied;
+//   7..  only gather: one SM issues scattered 16-byte copies faster with more warps issuing them
+//        (the CTA holds the whole SM, so the extra warps cost no occupancy).
 #include <cudaTypedefs.h>
 
 #include "tc.h"
@@ -40,7 +42,8 @@ constexpr int kD = 512;
 constexpr int kH = 64;
 constexpr int kTile = 128;
 constexpr int kMaxTiles = 2;                        // tiles per CTA
-constexpr int kThreads = 224;
+constexpr int kGatherOnlyWarps = 4;                // warps 7.. : gather only
+constexpr int kThreads = 224 + 32 * kGatherOnlyWarps;
 constexpr int kStages = 4;                          // = chunks per tile: chunk c always uses stage c
 constexpr uint32_t kBlk = kTile * 128;              // 16 KB: [128 rows][64 dims] swizzled
 constexpr uint32_t kChunkBytes = 2 * kBlk;          // 32 KB: 128 rows x 128 dims
@@ -51,7 +54,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = kMaxTiles * kH;          // O^T[dc] at kColO + 64 dc
 constexpr uint32_t kIdescS = idesc_bf16(128, 64, false, false);
 constexpr uint32_t kIdescO = idesc_bf16(128, 64, true, true);
-constexpr int kGatherThreads = 160;                 // warps 1..5
+constexpr int kGatherThreads = 160 + 32 * kGatherOnlyWarps;   // warps 1..5 and 7..
 constexpr size_t kAuxBytes = 2048;                   // barriers, row table, RoPE table (< 1.5 KB)
 constexpr size_t kSmemBytes = 1024 + kQBytes + kStages * kChunkBytes + kMaxTiles * kPBytes + kAuxBytes;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- the gather (warps 1..5)
   // Load i brings chunk c (dims 128c..128c+127) of the 128 rows of tile slot j into stage c: 2048
   // pieces of 16 bytes, consecutive threads on consecutive pieces of a row. Empty slots are zeros.
-  const int gt = threadIdx.x - 32;                             // gather thread 0..159 (warps 1..5)
+  const int gt = warp >= 7 ? threadIdx.x - 64 : threadIdx.x - 32;   // gather thread: warps 1..5, then 7..
   auto gather_issue = [&](int j, int c) {
     uint8_t* stage = ring + c * kChunkBytes;
     const __nv_bfloat16* base = is_win(j) ? p.kv : p.ckv;
@@ -305,8 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) mma_commit(bar_o);
       CSA_STAMP(11);
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- gather (warp 1 only gathers)
+  } else if (warp == 1 || warp >= 7) {
+    // ---------------------------------------------------------------- gather (these warps only gather)
     // Drain the S^T phase before the re-gather: its loads wait for the O^T MMAs, which need the
     // softmax, which needs every S^T phase load completed by all gather threads.
     bool ok = true;
