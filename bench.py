@@ -160,10 +160,28 @@ def dist_setup():
     if world > 1:
         import torch.distributed as dist
         torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist.init_process_group(dist_backend(), device_id=torch.device("cuda", local))
     elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return world, rank, local
+
+
+def dist_backend() -> str:
+    """NCCL between GPUs; gloo where there is none (the host-side tests of the multi-rank logic)."""
+    import torch
+    return "nccl" if torch.cuda.is_available() else "gloo"
+
+
+def rank_requests(rank: int, B: int) -> list[int]:
+    """The requests rank `rank` serves: its own B of them, so every rank's work is distinct (weak
+    scaling: the job's requests grow with the ranks, nothing is exchanged on the data path)."""
+    return list(range(rank * B, rank * B + B))
+
+
+def job_value(world: int, B: int, K: int, seconds_max: float) -> float:
+    """Whole-job query-tokens/s: every rank decodes B requests per step for K steps, and the job
+    takes as long as its slowest rank."""
+    return world * B * K / seconds_max
 
 
 def barrier(world):
@@ -177,7 +195,7 @@ def max_over_ranks(x: float, world: int) -> float:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -248,7 +266,7 @@ def run_decode(args, world, rank, device, peaks) -> dict:
     R = args.rotations
     cfg = make_cfg(wl)
     t_setup = time.time()
-    T = device_inputs(wl, list(range(rank * B, rank * B + B)), device)
+    T = device_inputs(wl, rank_requests(rank, B), device)
     cache = make_cache(T, wl, device)
     L.csa_compress(cfg, cache, 0, wl.n_entries)            # the caches the decode step reads
     pos = torch.full((B,), wl.t, dtype=torch.int64, device=device)
@@ -324,7 +342,7 @@ def run_decode(args, world, rank, device, peaks) -> dict:
     idx_avg_s = idx_ms / max(idx_n, 1) / 1e3
     achieved = work["index_bytes"] / idx_avg_s / 1e9 if idx_n else None
     step_s = ms_max / K / 1e3
-    qtok = world * B * K / (ms_max / 1e3)
+    qtok = job_value(world, B, K, ms_max / 1e3)
     res = {
         "value": qtok, "ms_per_step": ms_max / K, "hbm_gbs": work["bytes"] / step_s / 1e9,
         "hbm_frac_of_measured": work["bytes"] / step_s / 1e9 / peaks["hbm_gbs"],
@@ -458,7 +476,7 @@ def run_e2e(args, wl, rot, world, device) -> dict:
     el = time.perf_counter() - t0
     barrier(world)
     el = max_over_ranks(el, world)
-    return {"value": world * B * K / el, "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
+    return {"value": job_value(world, B, K, el), "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": el / K * 1e3,
             "how": "per step: one packed upload from pinned host memory (+ the raw rows placed into the "
                    "caches on the device), csa_decode, read-back to pinned host memory; one CUDA graph "
