@@ -180,6 +180,26 @@ def compress(kv, gate, bias, ratio: int, n_entries: int | None = None, *, rms_ep
     return out
 
 
+def compress_entry(kv_rows, gate_rows, bias, e: int, ratio: int, *, rms_eps: float = 1e-6,
+                   d_rope: int = 64, rope_base: float = 10000.0) -> np.ndarray:
+    """Entry e alone, from the raw rows of its own window: the same rule as ``compress`` for one
+    entry (pooling of tokens [(e-1)m, (e+1)m), RMSNorm, RoPE at position e*m), for spot checks of
+    long caches whose every entry would be too costly to recompute.
+
+    kv_rows/gate_rows: [2m, C] = tokens (e-1)m .. (e+1)m-1, or [m, C] = tokens 0 .. m-1 for e = 0
+    (the previous group does not exist: weight 0). Returns [C] float64.
+    """
+    m = ratio
+    kv_rows, gate_rows = _f64(kv_rows), _f64(gate_rows)
+    if e == 0:
+        assert kv_rows.shape[0] == m
+        kv_rows = np.concatenate([np.zeros_like(kv_rows), kv_rows])
+        gate_rows = np.concatenate([np.full_like(gate_rows, -np.inf), gate_rows])
+    assert kv_rows.shape[0] == 2 * m
+    x = rms_norm(pool_window(kv_rows, gate_rows, bias), rms_eps)
+    return rope(x, e * m, d_rope, rope_base)
+
+
 def visible(t: int, ratio: int) -> int:
     """Number of compressed entries a query at position t may read: (t+1)//ratio
     ([FLASH] "压缩条目必须等整组完成后才可见")."""

@@ -124,6 +124,20 @@ def test_compress_matches_per_entry_window_loop():
         np.testing.assert_allclose(got[i], want, rtol=1e-12, atol=1e-14)
 
 
+def test_compress_entry_equals_the_whole_sequence_form():
+    """The single-entry form (used for spot checks of long caches) against compress(): entry 0
+    (no previous group), interior entries and the last one, at large positions where RoPE
+    angles are far from zero."""
+    rng = np.random.default_rng(16)
+    m, C, N = 4, 64, 4096
+    kv, gate, bias = _rand(rng, N, C), _rand(rng, N, C), _rand(rng, 2 * m, C, s=0.3)
+    whole = O.compress(kv, gate, bias, m, d_rope=16)
+    for e in (0, 1, 2, 517, N // m - 1):
+        lo = max(0, (e - 1) * m)
+        got = O.compress_entry(kv[lo:(e + 1) * m], gate[lo:(e + 1) * m], bias, e, m, d_rope=16)
+        np.testing.assert_allclose(got, whole[e], rtol=1e-12, atol=1e-14)
+
+
 def test_pooling_weights_sum_to_one():
     """The pooled value of a constant column is that constant (weights sum to 1)."""
     rng = np.random.default_rng(7)
