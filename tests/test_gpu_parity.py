@@ -29,6 +29,9 @@ DECODE = {
     # the first groups: entry 0 closes at t = 3 (its previous group lies before position 0, weight
     # 0), entry 1 at t = 7; t = 0 and t = 2 see no compressed entry at all
     "csa_bf16_early": (synth.small_workload(1, wid=107, B=5, N=520, t=519), [3, 7, 2, 0, 519]),
+    # the Pro variant's selection size: 1024 selected entries (8 tiles) + the window per query
+    "csa_bf16_k1024": (synth.small_workload(1, wid=108, B=4, N=8195, t=8194, top_k=1024),
+                       [8194, 8191, 5000, 4095]),
 }
 MODES = [False, True]          # tensor-core path where available, then the CUDA-core path
 
