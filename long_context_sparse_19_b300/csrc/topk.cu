@@ -608,8 +608,9 @@ static int64_t first_level_chunks(int64_t n_cap) { return (n_cap + kCapSmall - 1
 
 size_t topk_workspace_bytes(int64_t rows, int64_t n_cap, int k) {
   // candidates of the intermediate levels: two ping-pong buffers of (key, index) pairs, each large
-  // enough for the first level's output
-  if (n_cap <= kCapSmall || k <= 0) return 0;
+  // enough for the first level's output. Rows of up to 16384 entries are selected in one launch
+  // (one CTA or one cluster) and need none.
+  if (n_cap <= (int64_t)kCluMax * kCluChunk || k <= 0) return 0;
   return 2 * (size_t)rows * first_level_chunks(n_cap) * k * 8;
 }
 
