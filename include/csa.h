@@ -150,8 +150,11 @@ csa_status csa_sparse_attn(const csa_config* cfg, int32_t B, int32_t S, const in
 
 /* One decode step of B requests, one query each at pos[b] ([FLASH] "压缩条目必须等整组完成后才可见"):
  * the caller has already written token t = pos[b] into the raw rows of `cache`. If t closes a
- * group ((t + 1) % ratio == 0) entry t / ratio of ckv (and cidx) is written first; then the
- * indexer, top-k (skipped for HCA) and the sparse attention run for the query at t.
+ * group ((t + 1) % ratio == 0) entry t / ratio of ckv (and cidx) is written before anything reads
+ * it (with bf16 storage and top_k > 0 the indexer kernel pools both entries itself, the index
+ * entry ahead of the tile that scores it); the indexer, top-k (skipped for HCA) and the sparse
+ * attention run for the query at t. Stream order holds as for any call: the first kernel starts
+ * after the caller's earlier work on `stream`.
  *   pos   [B] int64 (device); q [B, H, d]; q_idx [B, H_idx, d_idx]; w [B, H_idx] (NULL for HCA)
  *   out   [B, H, d] storage; topk_out [B, top_k] int32, nullable (the selection used). */
 csa_status csa_decode(const csa_config* cfg, int32_t B, const int64_t* pos, const csa_cache* cache,
