@@ -36,25 +36,37 @@ ROTATIONS = 3                      # input copies cycled between steps (defeats 
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 # DRAM bytes (read + write) of one decode indexer launch at the decode workload, from an ncu capture
 # (profiles/index_tc_decode_B32_N65536.md). They hold only for the kernel source they were taken
-# on: the roofline's "traffic" is null as soon as any of these files differs from that capture.
+# on: the roofline's "traffic" is null as soon as the code of any of these files differs from
+# that capture.
 INDEX_TRAFFIC = {"bytes_per_launch": 135505920 + 1793024,
                  "sources": ["long_context_sparse_19_b300/csrc/tc_index.cu",
                              "long_context_sparse_19_b300/csrc/tc_ptx.cuh",
                              "long_context_sparse_19_b300/csrc/common.cuh",
                              "long_context_sparse_19_b300/csrc/close_entry.cuh"],
-                 "sha256": "d8801a5686fc862504b08eccbcbfdf046dab4d7957fa6128568926819d96464b"}
+                 "sha256": "44f1dd8972b692fb2d8e71008b68383a0f1f30fdbce5fcbf6141fe2c685850b3"}
 # GPU sleep queued ahead of each profiled step, so that the host has submitted the whole step before
 # it starts and the per-kernel events time the GPU, not the host's launch rate (~250 us at 2 GHz)
 PROFILE_SLEEP_CYCLES = 500_000
 
 
-def index_traffic() -> int | None:
+def source_digest(paths) -> str:
+    """SHA-256 of the code of CUDA sources: // comments and blank lines do not count, so that a
+    comment edit does not void a counter taken on the same code."""
     import hashlib
+    import re
     h = hashlib.sha256()
-    for rel in INDEX_TRAFFIC["sources"]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
-    return INDEX_TRAFFIC["bytes_per_launch"] if h.hexdigest() == INDEX_TRAFFIC["sha256"] else None
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            for line in f:
+                code = re.sub(r"//.*", "", line).rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
+    return h.hexdigest()
+
+
+def index_traffic() -> int | None:
+    ok = source_digest(INDEX_TRAFFIC["sources"]) == INDEX_TRAFFIC["sha256"]
+    return INDEX_TRAFFIC["bytes_per_launch"] if ok else None
 
 
 def load_peaks() -> dict:

@@ -16,6 +16,14 @@
 //     sum_h w_h * relu(hi_h + lo_h) -> one coalesced fp32 score store.
 // The cache stream is the only large traffic (256 B per visible entry), so the kernel is bound by
 // HBM bandwidth; two CTAs share an SM (about 98 KB shared memory and 256 TMEM columns each).
+//
+// In a decode step this kernel is the first launch and also runs the compressor's close step
+// ([FLASH] "压缩是逐通道的 learned pooling": when t completes a group, entry t / m is pooled):
+// right after building the query, the epilogue threads of the CTA that scores the request's last
+// tile pool the new index entry, store it, order the store before the async proxy and release an
+// mbarrier that gates the TMA load of that tile; the CTA that owns tile 0 pools the new KV entry
+// (the attention reads it later) and takes one tile fewer to make up for it. A separate close
+// kernel would hold 64 SMs' registers while this kernel's CTAs wait to start.
 #include <cudaTypedefs.h>
 
 #include <mutex>
