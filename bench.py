@@ -115,6 +115,7 @@ def prefill_flops(wl: synth.Workload) -> dict:
 
 # ----------------------------------------------------------------------------- clocks during the run
 class ClockSampler:
+    PERIOD_MS = 20                        # several samples even inside a sub-second timed region
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -124,8 +125,8 @@ class ClockSampler:
         self.err = None
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
-                 "-i", gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(ClockSampler.PERIOD_MS), "-i", gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError as e:
             self.proc, self.err = None, str(e)
             return
@@ -152,7 +153,7 @@ class ClockSampler:
         if not inside:                           # region shorter than the sampling period
             near = sorted(self.samples, key=lambda x: min(abs(x[0] - t0), abs(x[0] - t1)))[:2]
             inside = [s for _, s in near]
-            note = "nearest samples (timed region shorter than the 100 ms sampling period)"
+            note = f"nearest samples (timed region shorter than the {self.PERIOD_MS} ms sampling period)"
         if not inside:
             return {"unavailable": "no nvidia-smi samples"}
         sm = [float(s[1]) for s in inside if s[1].replace(".", "").isdigit()]
@@ -643,7 +644,7 @@ def decode_config(world, args=None) -> dict:
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--prefill-reps", type=int, default=3)
