@@ -619,7 +619,9 @@ def run_reference(args, world, rank) -> None:
     line = {"metric": METRIC, "impl": "reference", "value": v, "unit": "query-tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": decode_config(world),
+            "data": "synthetic",
+            "config": dict(decode_config(world), timing="host wall clock around the oracle's decode steps",
+                           l2="not applicable (host)"),
             "cpu_baseline": {"value": v, "unit": "query-tokens/s", "kind": "oracle",
                              "cores": hc["blas_threads"] or hc["affinity_cores"],
                              "sample": f"each step = one request's decode step (requests 0..{n_req - 1} of the "
