@@ -263,11 +263,29 @@ csa_status run_compress(const csa_config* c, int B, const csa_cache* k, int64_t 
       "compress launch");
 }
 
+// Cluster size of the fused decode indexer + selection for this call, or 0 when it does not apply.
+int fused_select_cluster(const csa_config* c, int B, int S, int64_t n_cap) {
+  if (S != 1 || !use_tc_index(c)) return 0;
+  return tc_index_select_cluster(B, n_cap);
+}
+
+// `scores`: where the scores go; `scores_out`: the caller's score output (nullable), the only
+// scores the fused decode kernel writes (it keeps its own in shared memory).
 csa_status run_index_topk(const csa_config* c, int B, int S, const int64_t* pos, const void* q_idx,
                           const float* w, const void* cidx, int64_t n_cap, int32_t* topk,
-                          float* scores, void* tk_ws, void* tc_ws, cudaStream_t st, bool pdl,
-                          const CompressParams* close = nullptr) {
+                          float* scores, float* scores_out, void* tk_ws, void* tc_ws, cudaStream_t st,
+                          bool pdl, const CompressParams* close = nullptr) {
   const bool bf16 = c->storage == CSA_BF16;
+  const int clu = fused_select_cluster(c, B, S, n_cap);
+  if (clu > 0) {
+    const RopeTab rope = make_rope(c);
+    int32_t* err = device_error_word();
+    return cuda_status(launch_stage(ST_INDEX, st, [&] {
+                         return tc_index_select(B, clu, pos, q_idx, w, cidx, n_cap, c->ratio, c->top_k, rope,
+                                                scores_out, topk, err, st, pdl, close);
+                       }),
+                       "fused indexer + selection launch");
+  }
   if (use_tc_index(c)) {
     const RopeTab rope = make_rope(c);
     int32_t* err = device_error_word();
@@ -398,7 +416,7 @@ csa_status csa_index_topk(const csa_config* cfg, int32_t B, int32_t S, const int
   if (s != CSA_OK) return s;
   if (B == 0 || S == 0) return CSA_OK;
   float* sc = scores ? scores : carve<float>(ws, pl.off_scores);
-  return run_index_topk(cfg, B, S, pos, q_idx, w, cidx, n_cap, topk, sc, carve<char>(ws, pl.off_tksel),
+  return run_index_topk(cfg, B, S, pos, q_idx, w, cidx, n_cap, topk, sc, scores, carve<char>(ws, pl.off_tksel),
                         carve<char>(ws, pl.off_tc), stream, false);
 }
 
@@ -411,9 +429,13 @@ csa_status csa_index_topk_static(const csa_config* cfg, int32_t B, int32_t S, co
   if (B < 0 || B > 65535 || S < 0 || S > 65535) return fail(CSA_ERR_SHAPE, "B = %d, S = %d", B, S);
   if (n_cap < 1) return fail(CSA_ERR_SHAPE, "n_cap = %lld", (long long)n_cap);
   CHECK_PTR(pos); CHECK_PTR(q_idx); CHECK_PTR(w); CHECK_PTR(cidx); CHECK_PTR(topk); CHECK_OPT_PTR(scores);
-  // the indexer and selection use the front of the workspace plan: scores, selection, candidates
-  const Plan pl = make_plan(cfg, B, S, n_cap);
-  const size_t need = pl.off_tksel + topk_workspace_bytes((int64_t)B * S, n_cap, cfg->top_k);
+  // Scratch actually used: nothing on the fused decode path (scores stay on chip); otherwise the
+  // float32 scores when the caller passes none, then the candidate lists of long rows.
+  const bool fused = fused_select_cluster(cfg, B, S, n_cap) > 0;
+  const size_t rows = (size_t)B * (size_t)S;
+  const size_t sc_bytes = (fused || scores) ? 0 : up(rows * (size_t)n_cap * sizeof(float));
+  const size_t tk_bytes = fused ? 0 : topk_workspace_bytes((int64_t)rows, n_cap, cfg->top_k);
+  const size_t need = sc_bytes + tk_bytes;
   if (need > (size_t)CSA_STATIC_SCRATCH_BYTES)
     return fail(CSA_ERR_WORKSPACE,
                 "csa_index_topk_static: B = %d, S = %d, n_cap = %lld need %zu bytes of scratch, more than the "
@@ -423,8 +445,9 @@ csa_status csa_index_topk_static(const csa_config* cfg, int32_t B, int32_t S, co
   uint8_t* ws = static_scratch(&e);
   if (!ws) return cuda_status(e, "csa_index_topk_static: device address of the static scratch");
   if (B == 0 || S == 0) return CSA_OK;
-  float* sc = scores ? scores : reinterpret_cast<float*>(ws + pl.off_scores);
-  return run_index_topk(cfg, B, S, pos, q_idx, w, cidx, n_cap, topk, sc, ws + pl.off_tksel, nullptr, stream, false);
+  float* sc = scores ? scores : reinterpret_cast<float*>(ws);
+  return run_index_topk(cfg, B, S, pos, q_idx, w, cidx, n_cap, topk, sc, scores, ws + sc_bytes, nullptr, stream,
+                        false);
 }
 
 csa_status csa_sparse_attn(const csa_config* cfg, int32_t B, int32_t S, const int64_t* pos, const void* q,
@@ -471,8 +494,8 @@ csa_status csa_decode(const csa_config* cfg, int32_t B, const int64_t* pos, cons
   if (!hca) {
     tk = topk_out ? topk_out : carve<int32_t>(ws, pl.off_topk);
     s = run_index_topk(cfg, B, 1, pos, q_idx, w, cache->cidx, cache->n_cap, tk,
-                       carve<float>(ws, pl.off_scores), carve<char>(ws, pl.off_tksel), carve<char>(ws, pl.off_tc),
-                       stream, !fused_close, fused_close ? &close : nullptr);
+                       carve<float>(ws, pl.off_scores), nullptr, carve<char>(ws, pl.off_tksel),
+                       carve<char>(ws, pl.off_tc), stream, !fused_close, fused_close ? &close : nullptr);
     if (s != CSA_OK) return s;
   }
   return run_attn(cfg, pl, B, 1, pos, q, cache->kv, cache->N, cache->ckv, cache->n_cap, tk, sink, out, ws,
@@ -502,8 +525,8 @@ csa_status csa_prefill(const csa_config* cfg, int32_t B, int32_t S, const csa_ca
   if (!hca) {
     tk = topk_out ? topk_out : carve<int32_t>(ws, pl.off_topk);
     s = run_index_topk(cfg, B, S, nullptr, q_idx, w, cache->cidx, cache->n_cap, tk,
-                       carve<float>(ws, pl.off_scores), carve<char>(ws, pl.off_tksel), carve<char>(ws, pl.off_tc),
-                       stream, true);
+                       carve<float>(ws, pl.off_scores), nullptr, carve<char>(ws, pl.off_tksel),
+                       carve<char>(ws, pl.off_tc), stream, true);
     if (s != CSA_OK) return s;
   }
   return run_attn(cfg, pl, B, S, nullptr, q, cache->kv, cache->N, cache->ckv, cache->n_cap, tk, sink, out,

@@ -1,4 +1,4 @@
-// The decode compressor's closing entry, computed by 128 threads of a CTA that has other work.
+// The decode compressor's closing entry, computed by one group of threads of a CTA that has other work.
 //
 // [FLASH] "DeepSeek-V4-Flash 架构：一个 token 的旅程", sections "压缩是逐通道的 learned pooling" and
 // "一个通道，逐项算出压缩结果": when position t closes a group (t + 1 divisible by m), entry
@@ -15,12 +15,17 @@ namespace csa {
 
 template <int P>
 __device__ __forceinline__ void load_row_part(const __nv_bfloat16* p, float (&v)[P]) {
-  static_assert(P == 1 || P == 4, "1 or 4 channels per thread");
+  static_assert(P == 1 || P == 2 || P == 4 || P == 8, "1, 2, 4 or 8 channels per thread");
   if constexpr (P == 1) {
     v[0] = __bfloat162float(p[0]);
-  } else {
+  } else if constexpr (P == 2) {
+    const uint32_t u = __ldg(reinterpret_cast<const unsigned int*>(p));
+    v[0] = bf16lo(u); v[1] = bf16hi(u);
+  } else if constexpr (P == 4) {
     const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
     v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
+  } else {
+    load8(p, v);
   }
 }
 
@@ -28,23 +33,27 @@ template <int P>
 __device__ __forceinline__ void load_row_part(const float* p, float (&v)[P]) {
   if constexpr (P == 1) {
     v[0] = __ldg(p);
-  } else {
+  } else if constexpr (P == 2) {
+    const float2 f = __ldg(reinterpret_cast<const float2*>(p));
+    v[0] = f.x; v[1] = f.y;
+  } else if constexpr (P == 4) {
     const float4 f = __ldg(reinterpret_cast<const float4*>(p));
     v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+  } else {
+    load8(p, v);
   }
 }
 
-// Pools entry e of request b of `job` (C channels, bf16 rows) and stores it. Called by all 128
-// threads `tid` = 0..127 of one group, which synchronise on named barrier `bar_id`; `red` is 4
-// floats of shared memory. Returns after this thread's part of the entry is stored.
-template <int C>
+// Pools entry e of request b of `job` (C channels, bf16 rows) and stores it. Called by all kT
+// threads `tid` = 0..kT-1 of one group (whole warps), which synchronise on named barrier `bar_id`;
+// `red` is kT / 32 floats of shared memory. Returns after this thread's part of the entry is stored.
+template <int C, int kT = 128>
 __device__ __forceinline__ void close_entry_bf16(const CompressJob& job, int64_t N, int64_t n_cap, int m,
                                                  float eps, const RopeTab& rope, int64_t b, int64_t e, int tid,
                                                  float* red, int bar_id) {
-  constexpr int kT = 128;
   constexpr int P = C / kT;                      // channels per thread
-  static_assert(C % kT == 0 && (P == 1 || P == 4), "C = 128 or 512");
-  constexpr int kU = 8;                          // tokens whose loads are in flight together
+  static_assert(C % kT == 0 && (P == 1 || P == 2 || P == 4 || P == 8) && kT % 32 == 0, "channels per thread");
+  constexpr int kU = P >= 8 ? 4 : 8;             // tokens whose loads are in flight together
   const int c0 = tid * P;
   const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(job.src) + b * N * C + c0;
   const __nv_bfloat16* gate = static_cast<const __nv_bfloat16*>(job.gate) + b * N * C + c0;
@@ -91,7 +100,10 @@ __device__ __forceinline__ void close_entry_bf16(const CompressJob& job, int64_t
   ss = warp_sum(ss);
   if ((tid & 31) == 0) red[tid >> 5] = ss;
   named_barrier(bar_id, kT);
-  const float inv = 1.0f / sqrtf((red[0] + red[1] + red[2] + red[3]) / (float)C + eps);
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kT / 32; ++w) tot += red[w];
+  const float inv = 1.0f / sqrtf(tot / (float)C + eps);
 #pragma unroll
   for (int k = 0; k < P; ++k) x[k] *= inv;
   const int r0 = C - rope.d_rope;
@@ -114,10 +126,17 @@ __device__ __forceinline__ void close_entry_bf16(const CompressJob& job, int64_t
         x[2 * q + 1] = a * sn + bb * cs;
       }
     }
-    uint2 u;
-    u.x = pack_bf16(x[0], x[1]);
-    u.y = pack_bf16(x[2], x[3]);
-    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(job.dst) + (b * n_cap + e) * C + c0) = u;
+    __nv_bfloat16* d = static_cast<__nv_bfloat16*>(job.dst) + (b * n_cap + e) * C + c0;
+    if constexpr (P == 2) {
+      *reinterpret_cast<uint32_t*>(d) = pack_bf16(x[0], x[1]);
+    } else if constexpr (P == 4) {
+      uint2 u;
+      u.x = pack_bf16(x[0], x[1]);
+      u.y = pack_bf16(x[2], x[3]);
+      *reinterpret_cast<uint2*>(d) = u;
+    } else {
+      store8(d, x);
+    }
   }
 }
 

@@ -27,6 +27,15 @@ cudaError_t tc_index_scores(int B, int S, const int64_t* pos, const void* q_idx,
                             float* scores, void* ws, int32_t* err, cudaStream_t st, bool pdl,
                             const CompressParams* close = nullptr);
 
+// Decode indexer and selection fused (S = 1): one cluster of C CTAs per request scores its visible
+// entries and selects the top_k (ascending entry index, -1 padded) into topk [B, top_k]; scores
+// [B, n_cap] is written only when non-null. `close`: as for tc_index_scores.
+// tc_index_select_cluster gives C for B requests of capacity n_cap, or 0 when the kernel does not apply.
+int tc_index_select_cluster(int B, int64_t n_cap);
+cudaError_t tc_index_select(int B, int C, const int64_t* pos, const void* q_idx, const float* w, const void* cidx,
+                            int64_t n_cap, int ratio, int top_k, const RopeTab& rope, float* scores, int32_t* topk,
+                            int32_t* err, cudaStream_t st, bool pdl, const CompressParams* close = nullptr);
+
 // Many-query attention (prefill): one CTA per query over all of its candidates (at most
 // tc_attn_prefill_max_tiles() tiles of 128), final output written directly.
 int tc_attn_prefill_max_tiles();
