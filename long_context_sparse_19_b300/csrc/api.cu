@@ -187,6 +187,8 @@ size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 struct Plan {
   bool tc_attn = false;
   bool tc_prefill = false;           // one CTA per query over all candidates, no partials
+  int fused = 0;                     // decode: cluster size of the fused attention + merge (0: split path)
+  int f_wc = 0, f_kc = 0, f_rows = 0;
   int n_split = 1, split_len = 0;
   size_t off_scores = 0, off_topk = 0, off_tksel = 0, off_po = 0, off_pml = 0, off_tc = 0, total = 0;
 };
@@ -197,7 +199,12 @@ Plan make_plan(const csa_config* c, int B, int S, int64_t n_cap) {
   const int64_t c_max = (int64_t)c->window + (hca ? n_cap : c->top_k);
   if (S == 1) {                               // decode: split the candidates across CTAs
     p.tc_attn = use_tc_attn(c);
-    if (p.tc_attn) {
+    if (p.tc_attn && !hca) p.fused = tc_attn_fused_plan(B, c->window, c->top_k, &p.f_wc, &p.f_kc, &p.f_rows);
+    if (p.fused) {
+      p.tc_attn = false;                      // one cluster per query merges on chip: no partials
+      p.n_split = 1;
+      p.split_len = (int)c_max;
+    } else if (p.tc_attn) {
       p.split_len = tc_attn_split_len();
       p.n_split = tc_attn_splits(c->window, c->top_k, n_cap, B * S);
     } else {
@@ -218,7 +225,9 @@ Plan make_plan(const csa_config* c, int B, int S, int64_t n_cap) {
     p.off_topk = o;   o = up(o + rows * (size_t)c->top_k * sizeof(int32_t));
     p.off_tksel = o;  o = up(o + topk_workspace_bytes((int64_t)rows, n_cap, c->top_k));
   }
-  if (p.n_split > 1 || p.tc_attn) {
+  if (p.fused) {                              // fp16 partials of each CTA of a query's cluster
+    p.off_po = o;  o = up(o + tc_attn_fused_workspace(B, p.fused));
+  } else if (p.n_split > 1 || p.tc_attn) {
     p.off_po = o;  o = up(o + rows * p.n_split * (size_t)c->H * c->d * sizeof(float));
     p.off_pml = o; o = up(o + rows * p.n_split * (size_t)c->H * 2 * sizeof(float));
   }
@@ -274,7 +283,7 @@ int fused_select_cluster(const csa_config* c, int B, int S, int64_t n_cap) {
 csa_status run_index_topk(const csa_config* c, int B, int S, const int64_t* pos, const void* q_idx,
                           const float* w, const void* cidx, int64_t n_cap, int32_t* topk,
                           float* scores, float* scores_out, void* tk_ws, void* tc_ws, cudaStream_t st,
-                          bool pdl, const CompressParams* close = nullptr) {
+                          bool pdl, const CompressParams* close = nullptr, const void* ckv_prefetch = nullptr) {
   const bool bf16 = c->storage == CSA_BF16;
   const int clu = fused_select_cluster(c, B, S, n_cap);
   if (clu > 0) {
@@ -282,7 +291,7 @@ csa_status run_index_topk(const csa_config* c, int B, int S, const int64_t* pos,
     int32_t* err = device_error_word();
     return cuda_status(launch_stage(ST_INDEX, st, [&] {
                          return tc_index_select(B, clu, pos, q_idx, w, cidx, n_cap, c->ratio, c->top_k, rope,
-                                                scores_out, topk, err, st, pdl, close);
+                                                scores_out, topk, err, st, pdl, close, ckv_prefetch);
                        }),
                        "fused indexer + selection launch");
   }
@@ -320,6 +329,12 @@ csa_status run_attn(const csa_config* c, const Plan& pl, int B, int S, const int
   if (pl.n_split > 1 || pl.tc_attn) { ap.part_o = carve<float>(ws, pl.off_po); ap.part_ml = carve<float>(ws, pl.off_pml); }
   const bool bf16 = c->storage == CSA_BF16;
   cudaError_t e;
+  if (pl.fused) {
+    e = launch_stage(ST_ATTN, st, [&] {
+      return tc_attn_fused(B, pl.fused, pl.f_wc, pl.f_kc, pl.f_rows, ap, carve<char>(ws, pl.off_po), st, pdl);
+    });
+    return cuda_status(e, "fused decode attention launch");
+  }
   if (pl.tc_prefill) {
     e = launch_stage(ST_ATTN, st, [&] { return tc_attn_prefill(B, ap, st, pdl); });
     return cuda_status(e, "prefill attention launch");
@@ -495,7 +510,8 @@ csa_status csa_decode(const csa_config* cfg, int32_t B, const int64_t* pos, cons
     tk = topk_out ? topk_out : carve<int32_t>(ws, pl.off_topk);
     s = run_index_topk(cfg, B, 1, pos, q_idx, w, cache->cidx, cache->n_cap, tk,
                        carve<float>(ws, pl.off_scores), nullptr, carve<char>(ws, pl.off_tksel),
-                       carve<char>(ws, pl.off_tc), stream, !fused_close, fused_close ? &close : nullptr);
+                       carve<char>(ws, pl.off_tc), stream, !fused_close, fused_close ? &close : nullptr,
+                       pl.fused ? cache->ckv : nullptr);
     if (s != CSA_OK) return s;
   }
   return run_attn(cfg, pl, B, 1, pos, q, cache->kv, cache->N, cache->ckv, cache->n_cap, tk, sink, out, ws,

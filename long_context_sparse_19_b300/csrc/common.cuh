@@ -87,6 +87,23 @@ __device__ __forceinline__ void rope_cs(int64_t pos, const RopeTab& tab, int i, 
   rope_cs(pos, tab.th_hi[i], tab.th_lo[i], c, s);
 }
 
+// rope_cs out of line, (cos, sin) returned in registers: for code that runs once per CTA, where every
+// inlined copy of the sine / cosine evaluation is fetched from memory again
+static __device__ __noinline__ float2 rope_cs_nl(int64_t pos, float th_hi, float th_lo) {
+  float c, s;
+  rope_cs(pos, th_hi, th_lo, c, s);
+  return make_float2(c, s);
+}
+
+// 2^x by the hardware approximation (PTX ex2.approx.ftz.f32: relative error about 2^-22, 2^-inf = 0,
+// subnormal results flushed to zero). For softmax weights that are rounded to bf16 / fp16 next; the
+// library's exp2f also handles subnormal inputs and costs several times more per element.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------------------ reductions
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -169,6 +186,19 @@ __device__ __forceinline__ void dsmem_st(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void dsmem_st4(uint32_t addr, uint4 v) {   // addr 16-byte aligned
   asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w) : "memory");
+}
+
+// loads from another CTA's shared memory (a shared::cluster address from dsmem_addr)
+__device__ __forceinline__ float dsmem_ldf(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 dsmem_ld4f(uint32_t addr) {   // addr 16-byte aligned
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr) : "memory");
+  return v;
 }
 
 // ------------------------------------------------------------------ phase stamps

@@ -93,6 +93,9 @@ struct IndexSelParams {
   // the entry that t closes is pooled here (close.job[0].src non-null): KV entry by CTA 0, index
   // entry by the CTA that scores the last tile
   CompressParams close;
+  // [B, n_cap, 512] compressed KV rows, or null: each winner's row is requested into L2 as soon as it
+  // is known, so that the attention's gather of the selected rows finds them there
+  const __nv_bfloat16* ckv_prefetch;
 };
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -409,7 +412,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t m = key[u] & pmask;
     bool win = valid && (take_all || m > prefix);
     if (valid && !take_all && m == prefix) win = cpos++ < need;
-    if (win && slot < k) out[slot++] = (int32_t)(id0 + u);
+    if (win && slot < k) {
+      out[slot++] = (int32_t)(id0 + u);
+      if (p.ckv_prefetch) prefetch_l2(p.ckv_prefetch + ((int64_t)b * p.n_cap + id0 + u) * 512, 1024);
+    }
   }
   const uint32_t kk = min(k, n_valid);
   for (int j = (int)kk + (int)(rank * kThreads) + tid; j < p.k; j += (int)(C * kThreads)) out[j] = -1;
@@ -458,7 +464,8 @@ int tc_index_select_cluster(int B, int64_t n_cap) {
 
 cudaError_t tc_index_select(int B, int C, const int64_t* pos, const void* q_idx, const float* w, const void* cidx,
                             int64_t n_cap, int ratio, int top_k, const RopeTab& rope, float* scores, int32_t* topk,
-                            int32_t* err, cudaStream_t st, bool pdl, const CompressParams* close) {
+                            int32_t* err, cudaStream_t st, bool pdl, const CompressParams* close,
+                            const void* ckv_prefetch) {
   if (C < 1 || C > kCluMax || top_k < 1) return cudaErrorInvalidValue;
   const int64_t tiles = (n_cap + kTileM - 1) / kTileM;
   if ((tiles + C - 1) / C > kMaxTiles) return cudaErrorInvalidValue;
@@ -473,6 +480,7 @@ cudaError_t tc_index_select(int B, int C, const int64_t* pos, const void* q_idx,
   p.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
   p.w = w; p.scores = scores; p.topk = topk; p.pos = pos; p.n_cap = n_cap; p.ratio = ratio; p.k = top_k;
   p.rope = rope; p.err = err;
+  p.ckv_prefetch = static_cast<const __nv_bfloat16*>(ckv_prefetch);
   memset(&p.close, 0, sizeof p.close);
   if (close) {
     if (close->n_jobs != 2 || close->job[0].C != 512 || close->job[1].C != kDI) return cudaErrorInvalidValue;

@@ -67,10 +67,9 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Waits for the phase of `parity` to complete; after kWaitTimeoutNs it records DEVERR_TIMEOUT in
-// the error word and returns false so that the caller can leave its loop.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The slow path of mbar_wait, out of line: kernels that run a phase once per CTA pay for every
+// instruction they fetch, so the wait loop exists once per kernel instead of once per call site.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, int32_t* err) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -79,6 +78,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
       return false;
     }
   }
+}
+
+// Waits for the phase of `parity` to complete; after kWaitTimeoutNs it records DEVERR_TIMEOUT in
+// the error word and returns false so that the caller can leave its loop.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, err);
 }
 
 // mbar_wait for a whole warp: true only if every lane saw the phase complete. Use it in front of
