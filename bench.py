@@ -496,6 +496,156 @@ def run_e2e(args, wl, rot, world, device) -> dict:
                    "each on three streams, consecutive steps overlap; wall clock"}
 
 
+# ----------------------------------------------------------------------------- every decode workload
+EXTRA_WORKLOADS = (0, 3, 4)   # the tiny fp32 decode, HCA B=16 at N=262,144, and B=4 at N=1,048,576 (+3)
+
+
+def compress_bytes(wl: synth.Workload, B: int) -> int:
+    """Algorithmic bytes of a full-cache build: every raw token's rows read once (kv, gate and, for
+    CSA, idx_k, idx_gate) and every entry written once."""
+    es = 2 if wl.storage == "bf16" else 4
+    chans = wl.d + (0 if wl.hca else wl.d_idx)
+    n = wl.n_entries
+    return B * (n * wl.ratio * chans * 2 * es + n * chans * es)
+
+
+def time_graph(call, K: int, W: int) -> float:
+    """Milliseconds per replay of a CUDA graph of `call` (W untimed replays first)."""
+    import torch
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for _ in range(W):
+        g.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(K):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / K
+
+
+def run_decode_workload(cid: int, args, device, peaks) -> dict:
+    """One decode step of workload `cid` per step (CUDA graph of csa_decode), plus the full-cache
+    compressor build of the same workload and the oracle timed on the host beside it."""
+    import torch
+    import long_context_sparse_19_b300 as L
+    wl = synth.WORKLOADS[cid]
+    B = wl.B
+    cfg = make_cfg(wl)
+    T = device_inputs(wl, list(range(B)), device)
+    cache = make_cache(T, wl, device)
+    calls, keep, graphs = [], [], []
+    try:
+        # compressor: whole cache, CUDA events (second of two builds)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for rep in range(2):
+            torch.cuda.synchronize()
+            e0.record()
+            L.csa_compress(cfg, cache, 0, wl.n_entries)
+            e1.record()
+            torch.cuda.synchronize()
+        c_ms = e0.elapsed_time(e1)
+        c_bytes = compress_bytes(wl, B)
+        # decode: rotate over R copies of the compressed caches (and R positions) so that no step
+        # reads the previous step's compressed rows from L2 when a step's bytes fit in it
+        work = decode_work(wl, B)
+        R = 1 if work["bytes"] > 2 * 126e6 or wl.storage == "f32" else 4
+        # bind_decode captures raw device pointers: every tensor a call reads or writes stays
+        # referenced here for as long as the calls exist
+        calls, keep = [], []
+        for r in range(R):
+            t_r = wl.t - r * 2 * wl.ratio if R > 1 else wl.t
+            c = cache if r == 0 else L.Cache(kv=cache.kv, gate=cache.gate, gate_bias=cache.gate_bias,
+                                             ckv=cache.ckv.clone(), idx_k=cache.idx_k, idx_gate=cache.idx_gate,
+                                             idx_bias=cache.idx_bias,
+                                             cidx=None if wl.hca else cache.cidx.clone())
+            pos = torch.full((B,), t_r, dtype=torch.int64, device=device)
+            out = torch.empty(B, wl.H, wl.d, dtype=cache.kv.dtype, device=device)
+            ws = L.workspace(cfg, B, 1, wl.n_entries, device=device)
+            q = T["q"][:, 0].contiguous()
+            qi = None if wl.hca else T["q_idx"][:, 0].contiguous()
+            w = None if wl.hca else T["w"][:, 0].contiguous()
+            calls.append(L.binding.bind_decode(cfg, pos, c, q, qi, w, T["sink"], out, ws=ws))
+            keep.append((c, pos, out, ws, q, qi, w))
+        K = max(args.steps, 200)
+        if R == 1:
+            ms = time_graph(calls[0], K, max(args.warmup, 3))
+        else:                                     # one graph per copy, replayed in turn
+            graphs = []
+            for cl in calls:
+                cl()
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    cl()
+                graphs.append(g)
+            for i in range(max(args.warmup, 3)):
+                graphs[i % R].replay()
+            torch.cuda.synchronize()
+            e0.record()
+            for i in range(K):
+                graphs[i % R].replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / K
+        assert L.csa_get_device_status() == 0
+        step_s = ms / 1e3
+        gbs = work["bytes"] / step_s / 1e9
+        res = {"workload": wl.name, "B": B, "N": wl.N, "t": wl.t, "ratio": wl.ratio, "top_k": wl.top_k,
+               "storage": wl.storage, "value": B / step_s, "unit": "query-tokens/s", "ms_per_step": ms,
+               "steps": K, "step_bytes": work["bytes"], "hbm_gbs": gbs, "hbm_frac_of_measured": gbs / peaks["hbm_gbs"],
+               "l2": (f"compressed caches rotated over {R} copies and {R} positions" if R > 1 else
+                      ("one copy: the step's bytes exceed twice the 126 MB L2" if work["bytes"] > 2 * 126e6
+                       else "one copy: the step's 0.7 MB stay in L2 (a launch-bound workload)")),
+               "compress": {"ms": c_ms, "bytes": c_bytes, "gbs": c_bytes / c_ms / 1e6,
+                            "frac_of_measured": c_bytes / c_ms / 1e6 / peaks["hbm_gbs"],
+                            "entries": B * wl.n_entries}}
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline_workload(wl, T, cache, args.cpu_budget_extra)
+        return res
+    finally:
+        torch.cuda.synchronize()
+        calls, keep, graphs, T, cache = None, None, None, None, None
+        torch.cuda.empty_cache()
+
+
+def cpu_baseline_workload(wl, T, cache, budget_s: float) -> dict:
+    """The oracle's decode step of request 0 on the host, given its caches (copied from the device,
+    untimed; the oracle reads only the window of the raw rows, so those alone are copied)."""
+    from oracle import csa_oracle as O
+    o = O.OracleConfig(H=wl.H, d=wl.d, d_rope=wl.d_rope, H_idx=wl.H_idx, d_idx=wl.d_idx, ratio=wl.ratio,
+                       top_k=wl.top_k, window=wl.window)
+    t = wl.t
+    V = (t + 1) // wl.ratio
+    h64 = lambda x: x.detach().float().cpu().numpy().astype(np.float64)
+    kv = np.zeros((t + 1, wl.d))                  # left unbacked except the window
+    lo = max(0, t - wl.window + 1)
+    kv[lo:t + 1] = h64(T["kv"][0, lo:t + 1])
+    ckv = h64(cache.ckv[0, :V])
+    cidx = None if wl.hca else h64(cache.cidx[0, :V])
+    q = h64(T["q"][0, 0])
+    qi = None if wl.hca else h64(T["q_idx"][0, 0])
+    w = None if wl.hca else h64(T["w"][0, 0])
+    sink = h64(T["sink"])
+    O.decode_step(t, q, qi, w, sink, kv, ckv, cidx, o)          # warm-up
+    done, t0 = 0, time.perf_counter()
+    while True:
+        O.decode_step(t, q, qi, w, sink, kv, ckv, cidx, o)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    hc = host_cores()
+    return {"value": done / el, "unit": "query-tokens/s", "cores": hc["blas_threads"] or hc["affinity_cores"],
+            "kind": "oracle", "sample": f"{done} decode steps of request 0 (fp64 NumPy, caches from the device, "
+                                        f"untimed), {el:.1f} s"}
+
+
 # ----------------------------------------------------------------------------- prefill leg
 def run_prefill(args, device, peaks) -> dict:
     import torch
@@ -652,6 +802,9 @@ def main():
     ap.add_argument("--prefill-reps", type=int, default=3)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--cpu-budget-extra", type=float, default=3.0,
+                    help="seconds of oracle work beside each of the other decode workloads")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the other decode workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--B", type=int, default=0, help="requests per GPU (default: the workload's 32)")
@@ -676,6 +829,9 @@ def main():
         cpu = run_cpu_baseline(args.cpu_budget)
     dec = run_decode(args, world, rank, device, peaks)
     pre = None if args.no_prefill else run_prefill(args, device, peaks)
+    extra = None
+    if rank == 0 and not args.no_workloads:
+        extra = {synth.WORKLOADS[c].name: run_decode_workload(c, args, device, peaks) for c in EXTRA_WORKLOADS}
     if rank == 0:
         line = {"metric": METRIC, "value": dec["value"], "unit": "query-tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": dec["ms_per_step"],
@@ -686,7 +842,7 @@ def main():
                 "gpu_launches": dec["gpu_launches"], "clocks": dec["clocks"],
                 "detail": {k: dec[k] for k in ("step_bytes", "step_flops", "stage_sum_ms_per_step",
                                                "stages_ms_per_step", "stage_launches", "setup_s")},
-                "prefill": pre}
+                "prefill": pre, "workloads": extra}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -297,7 +297,8 @@ def bind_decode(cfg: Config, pos, cache: Cache, q, q_idx, w, sink, out, topk_out
             _ptr(topk_out, (B, cfg.top_k), torch.int32, "topk_out"),
             _ptr(ws, None, torch.uint8, "ws"), ws.numel())
     fn = load().csa_decode
-    keep = (c, k, ws)
+    # the call holds raw device pointers: keep every tensor they point into alive with it
+    keep = (c, k, ws, pos, cache, q, q_idx, w, sink, out, topk_out)
 
     def call(stream=None):
         _ = keep

@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < 32; ++h) {
           const float m = m_s[half * 32 + h];
-          const float e = (valid && m != -INFINITY) ? exp2f((sv[h] - m) * c2) : 0.f;
+          const float e = (valid && m != -INFINITY) ? fast_exp2((sv[h] - m) * c2) : 0.f;
           sv[h] = e;
           v[half * 32 + h] += e;
         }
