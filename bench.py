@@ -796,7 +796,9 @@ def decode_config(world, args=None) -> dict:
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 5000 for the GPU arm, 100 for the reference arm, whose "
+                         "step is a fp64 host decode step of about 50 ms)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--prefill-reps", type=int, default=3)
@@ -812,6 +814,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.steps is None:
+        args.steps = 100 if args.impl == "reference" else 5000
 
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))

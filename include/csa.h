@@ -24,6 +24,9 @@
  *    i < (t + 1) / ratio ([FLASH] "压缩条目必须等整组完成后才可见") and raw tokens
  *    max(0, t - window + 1) .. t.
  *  - q and q_idx are passed before RoPE; the library rotates them at t.
+ *  - The library looks up the device addresses of its own device variables (the error word, the
+ *    scratch of csa_index_topk_static) once per device and keeps them: resetting a device
+ *    (cudaDeviceReset) while the library is loaded is not supported.
  */
 #ifndef CSA_H_
 #define CSA_H_
@@ -44,13 +47,20 @@ typedef enum {
   CSA_ERR_WORKSPACE = 4,       /* ws_bytes smaller than csa_workspace_bytes()               */
   CSA_ERR_CUDA = 5,            /* a CUDA runtime call or launch failed                      */
   CSA_ERR_DEVICE = 6,          /* a kernel reported a device-side error (see error word)    */
-  CSA_ERR_NOT_IMPLEMENTED = 7  /* valid request that this build does not support            */
+  CSA_ERR_NOT_IMPLEMENTED = 7, /* valid request that this build does not support            */
+  CSA_ERR_DEVICE_TIMEOUT = 8   /* a kernel's bounded wait ran out (error word DEVERR 2)     */
 } csa_status;
 
 typedef enum { CSA_F32 = 0, CSA_BF16 = 1 } csa_dtype;
 
 /* csa_config.flags */
 #define CSA_FLAG_SIMT 1u       /* use the CUDA-core kernels even where a tcgen05 kernel exists */
+/* Test hook for the timeout path, never set in production: the one-launch decode indexer (bf16,
+ * one query per request) skips its first cache-tile load and gives each of its waits 2 ms instead
+ * of 1 s, so the waits run out, the kernel records the timeout in the device error word and
+ * returns; the call's selection is then meaningless and csa_sync_status reports
+ * CSA_ERR_DEVICE_TIMEOUT. */
+#define CSA_FLAG_TEST_STALL (1u << 30)
 
 /* Shape and hyper-parameters of one layer (tensor contract of [FLASH] "每个算子先对齐四个维度").
  * Supported: d = 512, d_rope = 64, d_idx = 128, 1 <= H <= 64, 1 <= H_idx <= 64,
@@ -98,9 +108,15 @@ const char* csa_status_string(csa_status s);
 const char* csa_last_error(void);
 
 /* Reads (and with reset != 0 clears) the device error word of the current device after
- * synchronising `stream`. Returns CSA_OK or CSA_ERR_DEVICE; *code (nullable) receives the
- * raw word (0 = no error; otherwise a CSA_DEVERR_* value from the kernels). */
+ * synchronising `stream`. Returns CSA_OK, CSA_ERR_DEVICE_TIMEOUT (a bounded wait ran out) or
+ * CSA_ERR_DEVICE (another device-side error); *code (nullable) receives the raw word (0 = no
+ * error, 1 = a selected index outside the visible entries, 2 = a wait ran out, 3 = a position
+ * outside the raw capacity). The first error since the last reset is the one kept. */
 csa_status csa_get_device_status(cudaStream_t stream, int reset, int32_t* code);
+
+/* Synchronises `stream` and returns the device status as csa_get_device_status(stream, 0, NULL)
+ * does, leaving the error word as it is. */
+csa_status csa_sync_status(cudaStream_t stream);
 
 /* Workspace bytes needed by csa_index_topk / csa_sparse_attn / csa_decode / csa_prefill for
  * B requests, S queries per request and a compressed capacity of n_cap entries. Returns 0 for

@@ -18,9 +18,11 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcsa.so")
 
 CSA_F32, CSA_BF16 = 0, 1
 CSA_FLAG_SIMT = 1
+CSA_FLAG_TEST_STALL = 1 << 30          # timeout test hook (include/csa.h)
+CSA_ERR_DEVICE, CSA_ERR_DEVICE_TIMEOUT = 6, 8
 
 # the public entry points declared in include/csa.h
-EXPORTS = ("csa_status_string", "csa_last_error", "csa_get_device_status", "csa_workspace_bytes",
+EXPORTS = ("csa_status_string", "csa_last_error", "csa_get_device_status", "csa_sync_status", "csa_workspace_bytes",
            "csa_compress", "csa_index_topk", "csa_index_topk_static", "csa_sparse_attn", "csa_decode",
            "csa_prefill",
            "csa_launch_count", "csa_profile_begin", "csa_profile_end")
@@ -61,6 +63,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.csa_status_string.argtypes, L.csa_status_string.restype = [c_int], c_char_p
     L.csa_last_error.argtypes, L.csa_last_error.restype = [], c_char_p
     L.csa_get_device_status.argtypes, L.csa_get_device_status.restype = [vp, c_int, POINTER(c_int32)], c_int
+    L.csa_sync_status.argtypes, L.csa_sync_status.restype = [vp], c_int
     L.csa_workspace_bytes.argtypes, L.csa_workspace_bytes.restype = [cp, c_int32, c_int32, c_int64], c_size_t
     L.csa_compress.argtypes, L.csa_compress.restype = [cp, c_int32, POINTER(CsaCache), c_int64, c_int64, vp], c_int
     L.csa_index_topk.argtypes = [cp, c_int32, c_int32, vp, vp, vp, vp, c_int64, vp, vp, vp, c_size_t, vp]
@@ -105,6 +108,7 @@ class Config:
     rms_eps: float = 1e-6
     storage: str = "bf16"
     simt: bool = False
+    test_stall: bool = False           # the timeout test hook; never set in production
 
     @property
     def dtype(self) -> torch.dtype:
@@ -114,7 +118,7 @@ class Config:
         return CsaConfig(self.H, self.d, self.d_rope, self.H_idx, self.d_idx, self.ratio, self.top_k,
                          self.window, self.rope_base, self.softmax_scale, self.rms_eps,
                          CSA_BF16 if self.storage == "bf16" else CSA_F32,
-                         CSA_FLAG_SIMT if self.simt else 0)
+                         (CSA_FLAG_SIMT if self.simt else 0) | (CSA_FLAG_TEST_STALL if self.test_stall else 0))
 
 
 def _ptr(t, shape=None, dtype=None, name="tensor"):
@@ -177,6 +181,12 @@ def csa_get_device_status(reset: bool = True, stream=None) -> int:
     code = c_int32(0)
     load().csa_get_device_status(_stream(stream), int(reset), ctypes.byref(code))
     return code.value
+
+
+def csa_sync_status(stream=None) -> int:
+    """Synchronises the stream and returns the device status (0 = CSA_OK, CSA_ERR_DEVICE_TIMEOUT,
+    CSA_ERR_DEVICE); the device error word is left as it is."""
+    return int(load().csa_sync_status(_stream(stream)))
 
 
 def csa_workspace_bytes(cfg: Config, B: int, S: int, n_cap: int) -> int:

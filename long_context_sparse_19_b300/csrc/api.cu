@@ -291,7 +291,8 @@ csa_status run_index_topk(const csa_config* c, int B, int S, const int64_t* pos,
     int32_t* err = device_error_word();
     return cuda_status(launch_stage(ST_INDEX, st, [&] {
                          return tc_index_select(B, clu, pos, q_idx, w, cidx, n_cap, c->ratio, c->top_k, rope,
-                                                scores_out, topk, err, st, pdl, close, ckv_prefetch);
+                                                scores_out, topk, err, st, pdl, close, ckv_prefetch,
+                                                (c->flags & CSA_FLAG_TEST_STALL) != 0);
                        }),
                        "fused indexer + selection launch");
   }
@@ -371,6 +372,7 @@ const char* csa_status_string(csa_status s) {
     case CSA_ERR_CUDA: return "CUDA error";
     case CSA_ERR_DEVICE: return "device-side error";
     case CSA_ERR_NOT_IMPLEMENTED: return "not implemented";
+    case CSA_ERR_DEVICE_TIMEOUT: return "a device-side wait ran out";
   }
   return "unknown status";
 }
@@ -392,8 +394,11 @@ csa_status csa_get_device_status(cudaStream_t stream, int reset, int32_t* code) 
     if (s != CSA_OK) return s;
   }
   if (code) *code = v;
-  return v ? CSA_ERR_DEVICE : CSA_OK;
+  if (!v) return CSA_OK;
+  return v == DEVERR_TIMEOUT ? CSA_ERR_DEVICE_TIMEOUT : CSA_ERR_DEVICE;
 }
+
+csa_status csa_sync_status(cudaStream_t stream) { return csa_get_device_status(stream, 0, nullptr); }
 
 size_t csa_workspace_bytes(const csa_config* cfg, int32_t B, int32_t S, int64_t n_cap) {
   if (check_config(cfg) != CSA_OK || B < 0 || S < 0 || n_cap < 0) return 0;

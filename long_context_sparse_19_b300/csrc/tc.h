@@ -31,12 +31,13 @@ cudaError_t tc_index_scores(int B, int S, const int64_t* pos, const void* q_idx,
 // entries and selects the top_k (ascending entry index, -1 padded) into topk [B, top_k]; scores
 // [B, n_cap] is written only when non-null. `close`: as for tc_index_scores. `ckv_prefetch`
 // (nullable): the compressed KV cache, whose selected rows are requested into L2 once selected.
+// `test_stall`: the timeout test hook (csa.h, CSA_FLAG_TEST_STALL).
 // tc_index_select_cluster gives C for B requests of capacity n_cap, or 0 when the kernel does not apply.
 int tc_index_select_cluster(int B, int64_t n_cap);
 cudaError_t tc_index_select(int B, int C, const int64_t* pos, const void* q_idx, const float* w, const void* cidx,
                             int64_t n_cap, int ratio, int top_k, const RopeTab& rope, float* scores, int32_t* topk,
                             int32_t* err, cudaStream_t st, bool pdl, const CompressParams* close = nullptr,
-                            const void* ckv_prefetch = nullptr);
+                            const void* ckv_prefetch = nullptr, bool test_stall = false);
 
 // Many-query attention (prefill): one CTA per query over all of its candidates (at most
 // tc_attn_prefill_max_tiles() tiles of 128), final output written directly.

@@ -446,15 +446,17 @@ static int attn_tiles(int window, int top_k, int64_t n_cap) {
   return wt + (int)ct;
 }
 
-// Tiles per CTA: one (no tile is ever gathered twice) while the batch's tiles fit two waves of
-// CTAs - the first wave is mostly window tiles, which run during the selection kernel - else two.
-static int attn_tiles_per_cta(int rows, int tiles) {
-  return (int64_t)rows * tiles <= 2 * (int64_t)tc_sm_count() ? 1 : 2;
+// Tiles per CTA: one (no tile is ever gathered twice) while the batch's tiles fit in the waves the
+// launch can overlap with earlier work, else two. With a selection (CSA) the window tiles, listed
+// first, run during the selection kernel, so two waves of one-tile CTAs still pay off; without one
+// (HCA) every tile waits for the same closing step, so the CTAs must fit one wave (one per SM).
+static int attn_tiles_per_cta(int rows, int tiles, bool selection) {
+  return (int64_t)rows * tiles <= (selection ? 2 : 1) * (int64_t)tc_sm_count() ? 1 : 2;
 }
 
 int tc_attn_splits(int window, int top_k, int64_t n_cap, int rows) {
   const int tiles = attn_tiles(window, top_k, n_cap);
-  const int per = attn_tiles_per_cta(rows, tiles);
+  const int per = attn_tiles_per_cta(rows, tiles, top_k > 0);
   return (tiles + per - 1) / per;
 }
 
@@ -467,7 +469,7 @@ cudaError_t tc_sparse_attn(int B, const AttnParams& a, void*, cudaStream_t st, b
   }
   const int rows = B * a.S;
   const int tiles = attn_tiles(a.window, a.k, a.n_cap);
-  const int per = attn_tiles_per_cta(rows, tiles);
+  const int per = attn_tiles_per_cta(rows, tiles, a.k > 0);
   if (a.n_split != (tiles + per - 1) / per || !a.part_o) return cudaErrorInvalidValue;
   if ((int64_t)B * a.N >= (int64_t)1 << 31 || (int64_t)B * a.n_cap >= (int64_t)1 << 31) return cudaErrorInvalidValue;
   CUtensorMap qmap;

@@ -96,6 +96,9 @@ struct IndexSelParams {
   // [B, n_cap, 512] compressed KV rows, or null: each winner's row is requested into L2 as soon as it
   // is known, so that the attention's gather of the selected rows finds them there
   const __nv_bfloat16* ckv_prefetch;
+  // timeout test hook: skip the first cache-tile load and wait at most wait_ns (else 1 s)
+  int test_stall;
+  uint64_t wait_ns;
 };
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -204,8 +207,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages;
-        if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1, p.err)) break;
-        if (close_idx && i == ntiles - 1 && !mbar_wait(closed, 0, p.err)) break;   // holds entry e
+        if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1, p.err, p.wait_ns)) break;
+        if (close_idx && i == ntiles - 1 && !mbar_wait(closed, 0, p.err, p.wait_ns)) break;   // holds entry e
+        if (p.test_stall && i == 0) continue;                // the timeout test hook
         mbar_arrive_expect_tx(&full[st], kTileBytes);
         const int32_t y = (int32_t)(b * p.n_cap + (tile0 + i) * kTileM);
         uint8_t* dst = stage_base + st * kTileBytes;
@@ -216,17 +220,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // no copy may still be landing in the ring when the selection reuses it (after a wait that
       // ran out, loads can be left unconsumed): wait, bounded, for the last load of every stage
       for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-        mbar_wait(&full[i % kStages], (i / kStages) & 1, p.err);
+        if (!(p.test_stall && i == 0)) mbar_wait(&full[i % kStages], (i / kStages) & 1, p.err, p.wait_ns);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0 && ntiles > 0 && mbar_wait(qready, 0, p.err)) {
+    if (lane == 0 && ntiles > 0 && mbar_wait(qready, 0, p.err, p.wait_ns)) {
       tc_fence_after();
       const uint32_t q_addr = smem_u32(qop);
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages, acc = i & 1;
-        if (!mbar_wait(&full[st], (i / kStages) & 1, p.err)) break;
-        if (i >= 2 && !mbar_wait(&tempty[acc], ((i >> 1) & 1) ^ 1, p.err)) break;
+        if (!mbar_wait(&full[st], (i / kStages) & 1, p.err, p.wait_ns)) break;
+        if (i >= 2 && !mbar_wait(&tempty[acc], ((i >> 1) & 1) ^ 1, p.err, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t a_addr = smem_u32(stage_base + st * kTileBytes);
         const uint32_t d = tmem + acc * 128;
@@ -282,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* gout = p.scores ? p.scores + (int64_t)b * p.n_cap : nullptr;
     for (int i = 0; i < ntiles; ++i) {
       const int acc = i & 1;
-      if (!mbar_wait_warp(&tfull[acc], (i >> 1) & 1, p.err)) break;    // uniform over the warp
+      if (!mbar_wait_warp(&tfull[acc], (i >> 1) & 1, p.err, p.wait_ns)) break;    // uniform over the warp
       tc_fence_after();
       const uint32_t ta = tmem + ((quad * 32) << 16) + acc * 128;
       float s = 0.f;
@@ -465,7 +469,7 @@ int tc_index_select_cluster(int B, int64_t n_cap) {
 cudaError_t tc_index_select(int B, int C, const int64_t* pos, const void* q_idx, const float* w, const void* cidx,
                             int64_t n_cap, int ratio, int top_k, const RopeTab& rope, float* scores, int32_t* topk,
                             int32_t* err, cudaStream_t st, bool pdl, const CompressParams* close,
-                            const void* ckv_prefetch) {
+                            const void* ckv_prefetch, bool test_stall) {
   if (C < 1 || C > kCluMax || top_k < 1) return cudaErrorInvalidValue;
   const int64_t tiles = (n_cap + kTileM - 1) / kTileM;
   if ((tiles + C - 1) / C > kMaxTiles) return cudaErrorInvalidValue;
@@ -481,6 +485,8 @@ cudaError_t tc_index_select(int B, int C, const int64_t* pos, const void* q_idx,
   p.w = w; p.scores = scores; p.topk = topk; p.pos = pos; p.n_cap = n_cap; p.ratio = ratio; p.k = top_k;
   p.rope = rope; p.err = err;
   p.ckv_prefetch = static_cast<const __nv_bfloat16*>(ckv_prefetch);
+  p.test_stall = test_stall ? 1 : 0;
+  p.wait_ns = test_stall ? 2000000ull : kWaitTimeoutNs;
   memset(&p.close, 0, sizeof p.close);
   if (close) {
     if (close->n_jobs != 2 || close->job[0].C != 512 || close->job[1].C != kDI) return cudaErrorInvalidValue;

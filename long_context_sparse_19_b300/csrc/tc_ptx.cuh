@@ -69,29 +69,32 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 // The slow path of mbar_wait, out of line: kernels that run a phase once per CTA pay for every
 // instruction they fetch, so the wait loop exists once per kernel instead of once per call site.
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, int32_t* err) {
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, int32_t* err, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) {
+    if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) {
       set_error(err, DEVERR_TIMEOUT);
       return false;
     }
   }
 }
 
-// Waits for the phase of `parity` to complete; after kWaitTimeoutNs it records DEVERR_TIMEOUT in
-// the error word and returns false so that the caller can leave its loop.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
+// Waits for the phase of `parity` to complete; after `limit_ns` (kWaitTimeoutNs unless a test
+// shortens it) it records DEVERR_TIMEOUT in the error word and returns false so that the caller
+// can leave its loop.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err,
+                                          uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, err);
+  return mbar_wait_slow(bar, parity, err, limit_ns);
 }
 
 // mbar_wait for a whole warp: true only if every lane saw the phase complete. Use it in front of
 // warp-collective tcgen05 instructions (tcgen05.ld is .sync.aligned: every lane of the warp must
 // execute it together, so no lane may skip it on its own).
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int32_t* err) {
-  const bool ok = mbar_wait(bar, parity, err);
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int32_t* err,
+                                               uint64_t limit_ns = kWaitTimeoutNs) {
+  const bool ok = mbar_wait(bar, parity, err, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -30,6 +30,7 @@ def test_every_declared_function_is_exported():
 def test_status_strings():
     assert L.csa_status_string(0) == "ok"
     assert L.csa_status_string(4) == "workspace too small"
+    assert L.csa_status_string(8) == "a device-side wait ran out"
     assert L.csa_status_string(99) == "unknown status"
 
 

@@ -2,15 +2,16 @@
 
 The decode workloads (B=32 at N=65,536; HCA B=16 at N=262,144 with m=128; B=4 at N=1,048,579
 with a trailing incomplete group) and the S=8192 causal prefill run through the public calls on
-the seeded synthetic inputs. The oracle cannot redo every request at these sizes, so it checks
-samples, one by one:
+the seeded synthetic inputs. The oracle checks, one by one:
   * compressed entries (the first, the last, random ones and the entry the decode step closes,
     which is poisoned with NaN beforehand so that only the decode step can have written it),
     against the oracle's single-entry form on the same raw rows;
-  * the selection of sampled requests / queries, against the oracle's exact selection of its own
-    fp64 scores of the GPU's index cache (stage-chained), with the tie band of the tolerances;
+  * the selection of every decode request and of 256 or more prefill queries (group boundaries
+    around sampled points included), against the oracle's exact selection of its own fp64 scores
+    of the GPU's index cache (stage-chained), with the tie band of the tolerances;
   * the attention output of those requests / queries, against the oracle on the GPU's selection
-    and compressed entries.
+    and compressed entries;
+  * one request of the B=32 decode end to end from its raw inputs (the oracle's own caches).
 The raw rows the oracle reads are copied back from the device: they are the synthetic inputs
 (bf16 values drawn by the seeded generator), not results of the CUDA path. Host arrays the oracle
 indexes by position are zero-initialised (left unbacked by the OS) and filled only where read.
@@ -109,6 +110,7 @@ def test_full_size_decode_sampled(cid):
         for b in (0, B - 1):
             entries = sorted({0, 1, n - 1, *rng.integers(0, n, 6).tolist()} | ({e_close} if closes else set()))
             _check_entries_sampled(wl, T, cache, b, entries, wl.name)
+        for b in range(B):                              # the selection and output of every request
             sel = None if wl.hca else topk[b].cpu().numpy()
             _check_query(wl, o, T, cache, b, 0, t, sel, Hn.host64(out[b]), wl.name)
     finally:
@@ -133,9 +135,70 @@ def test_full_size_prefill_sampled():
         rng = np.random.default_rng(2)
         n = wl.n_entries
         _check_entries_sampled(wl, T, cache, 0, sorted({0, 1, n - 1, *rng.integers(0, n, 6).tolist()}), wl.name)
-        # group boundaries (3 -> 4 tokens makes entry 0 visible), the window edge, the last query
-        for t in sorted({0, 2, 3, 4, 127, 128, 2047, 2048, 4095, wl.S - 1, *rng.integers(0, wl.S, 4).tolist()}):
-            _check_query(wl, o, T, cache, 0, t, t, topk[0, t].cpu().numpy(), Hn.host64(out[0, t]), wl.name)
+        # group boundaries (3 -> 4 tokens makes entry 0 visible), the window edge, the last query,
+        # and around 24 sampled points every query from two groups before to two groups after
+        # (each crosses group boundaries): 256 queries or more
+        ts = {0, 1, 2, 3, 4, 5, 7, 8, 126, 127, 128, 129, 2047, 2048, 4095, 4096, wl.S - 1}
+        for p0 in rng.integers(8, wl.S - 8, 24).tolist():
+            ts |= set(range(p0 - 2 * wl.ratio, p0 + 2 * wl.ratio + 1))
+        ts = sorted(t for t in ts if 0 <= t < wl.S)
+        assert len(ts) >= 256
+        outh = Hn.host64(out[0, ts])
+        tk = topk[0, ts].cpu().numpy()
+        for i, t in enumerate(ts):
+            _check_query(wl, o, T, cache, 0, t, t, tk[i], outh[i], wl.name)
+    finally:
+        del T
+        torch.cuda.empty_cache()
+
+
+def test_full_size_decode_end_to_end():
+    """One request of the B = 32, N = 65,536 decode through the oracle from its raw inputs, not
+    stage-chained: the oracle compresses all 65,536 tokens itself (fp64), and
+      * every compressed entry of the GPU's caches is within one bf16 rounding of the oracle's;
+      * the GPU's selection equals the oracle's selection on the oracle's own caches, except swaps
+        among entries whose oracle scores lie within the bf16 cache-rounding band of the k-th
+        score (the selection is made on caches that differ by one rounding, so near-ties can swap);
+      * the GPU's output equals the oracle's attention over the oracle's caches for that selection.
+    The raw rows are the synthetic inputs copied back from the device."""
+    L = Hn.lib()
+    bench = _bench()
+    wl = synth.WORKLOADS[1]
+    c, o = Hn.configs(wl)
+    B, t, m = wl.B, wl.t, wl.ratio
+    T = bench.device_inputs(wl, list(range(B)), "cuda")
+    try:
+        cache = bench.make_cache(T, wl, "cuda")
+        L.csa_compress(c, cache, 0, wl.n_entries)
+        e_close = t // m
+        cache.ckv[:, e_close] = float("nan")
+        cache.cidx[:, e_close] = float("nan")
+        pos = torch.full((B,), t, dtype=torch.int64, device="cuda")
+        out = torch.full((B, c.H, c.d), float("nan"), dtype=c.dtype, device="cuda")
+        topk = torch.full((B, c.top_k), -7, dtype=torch.int32, device="cuda")
+        L.csa_decode(c, pos, cache, T["q"][:, 0], T["q_idx"][:, 0], T["w"][:, 0], T["sink"], out, topk)
+        torch.cuda.synchronize()
+        assert L.csa_get_device_status() == 0
+        b = 0
+        bias, ibias = Hn.host64(T["bias"]), Hn.host64(T["idx_bias"])
+        kv = Hn.host64(T["kv"][b])
+        ckv_o = O.compress(kv, Hn.host64(T["gate"][b]), bias, m, wl.n_entries)
+        cidx_o = O.compress(Hn.host64(T["idx_k"][b]), Hn.host64(T["idx_gate"][b]), ibias, m, wl.n_entries)
+        Hn.check_entries(Hn.host64(cache.ckv[b]), ckv_o, "bf16", "end-to-end ckv")
+        Hn.check_entries(Hn.host64(cache.cidx[b]), cidx_o, "bf16", "end-to-end cidx")
+        q, q_idx, w = (Hn.host64(T[k][b, 0]) for k in ("q", "q_idx", "w"))
+        sink = Hn.host64(T["sink"])
+        ref_s = O.index_scores(q_idx, w, cidx_o, t, m)
+        want = O.topk_select(ref_s, c.top_k)
+        got = topk[b].cpu().numpy()
+        sk = ref_s[want[-1]]
+        band = 2.0 ** -7 * max(abs(sk), float(np.sqrt(np.mean(ref_s * ref_s))))
+        diff = set(int(i) for i in got) ^ set(int(i) for i in want)
+        assert len(diff) <= 16, f"{len(diff)} entries differ from the oracle's own selection"
+        for i in diff:
+            assert abs(ref_s[i] - sk) <= band, f"entry {i}: score {ref_s[i]:.6g} outside the band around {sk:.6g}"
+        ref = O.sparse_attn(q, kv, ckv_o, got, sink, t, o)
+        Hn.check_attn(Hn.host64(out[b]), ref, "bf16", "end-to-end attention")
     finally:
         del T
         torch.cuda.empty_cache()

@@ -220,6 +220,61 @@ def test_prefill_matches_oracle(name, simt):
             Hn.check_attn(outh[b, t], ref, wl.storage, f"{name} prefill b{b} t{t}")
 
 
+CHUNKED = {
+    "csa_bf16": synth.small_workload(2, wid=206, B=2, N=1300, S=1300, top_k=64),
+    "hca_bf16": synth.small_workload(2, wid=207, B=2, N=1300, S=1300, ratio=16, top_k=0),
+    "csa_f32": synth.small_workload(2, wid=208, B=2, N=1300, S=1300, H=8, H_idx=8, top_k=32, storage="f32"),
+}
+
+
+@pytest.mark.parametrize("simt", MODES)
+@pytest.mark.parametrize("name", list(CHUNKED))
+def test_chunked_prefill_matches_oracle(name, simt):
+    """A prefill chunk over an existing cache ([FLASH] "压缩条目必须等整组完成后才可见": every query keeps
+    its own visibility): the entries of tokens 0..1023 exist, the chunk's tokens 1024..1299 close
+    further groups (csa_compress on the new entry range), then S queries of the chunk at
+    non-consecutive positions (each request its own order) go through csa_index_topk and
+    csa_sparse_attn with S > 1. Compared with the oracle on the GPU's caches."""
+    wl = CHUNKED[name]
+    bt = Hn.DeviceBatch(wl)
+    c, o = Hn.configs(wl, simt)
+    L = Hn.lib()
+    m = c.ratio
+    n0, n1 = 1024 // m, wl.N // m
+    L.csa_compress(c, bt.cache(), 0, n0)
+    L.csa_compress(c, bt.cache(), n0, n1 - n0)
+    rng = np.random.default_rng(len(name) + simt)
+    S = 12
+    P = np.stack([rng.permutation(np.arange(1024, wl.N))[:S] for _ in range(bt.B)]).astype(np.int64)
+    P[0, :3] = [wl.N - 1, 1024, 1027]                    # the chunk's last token and its first group
+    Pd = torch.from_numpy(P).cuda()
+    pick = lambda T: torch.stack([T[b, Pd[b]] for b in range(bt.B)]).contiguous()
+    q = pick(bt.q)
+    topk = None
+    if not o.hca:
+        topk = torch.full((bt.B, S, c.top_k), -7, dtype=torch.int32, device="cuda")
+        L.csa_index_topk(c, Pd, pick(bt.q_idx), pick(bt.w), bt.cidx, topk)
+    out = torch.full((bt.B, S, c.H, c.d), float("nan"), dtype=c.dtype, device="cuda")
+    L.csa_sparse_attn(c, Pd, q, bt.kv, bt.ckv, topk, bt.sink, out)
+    torch.cuda.synchronize()
+    assert L.csa_get_device_status() == 0
+    ref_caches = _oracle_caches(bt, o)
+    ckv, cidx = Hn.host64(bt.ckv), None if o.hca else Hn.host64(bt.cidx)
+    for b in range(bt.B):
+        Hn.check_entries(ckv[b, :n1], ref_caches[b][0][:n1], wl.storage, f"{name} chunk ckv[{b}]")
+        if cidx is not None:
+            Hn.check_entries(cidx[b, :n1], ref_caches[b][1][:n1], wl.storage, f"{name} chunk cidx[{b}]")
+        for s in range(S):
+            t = int(P[b, s])
+            sel = None
+            if not o.hca:
+                sel = topk[b, s].cpu().numpy()
+                ref_s = O.index_scores(bt.reqs[b]["q_idx"][t], bt.reqs[b]["w"][t], cidx[b], t, c.ratio)
+                Hn.check_topk_vs_oracle(sel, ref_s, c.top_k, f"{name} chunk b{b} t{t}")
+            ref = O.sparse_attn(bt.reqs[b]["q"][t], bt.reqs[b]["kv"], ckv[b], sel, bt.shared["sink"], t, o)
+            Hn.check_attn(Hn.host64(out[b, s]), ref, wl.storage, f"{name} chunk b{b} t{t}")
+
+
 @pytest.mark.parametrize("name", ["csa_bf16", "csa_f32"])
 def test_prefill_equals_decode_on_gpu(name):
     """The GPU's prefill rows equal its own decode steps at the same positions (prefill ==
@@ -253,6 +308,39 @@ def test_bad_selected_index_sets_device_error():
     assert L.csa_get_device_status(reset=True) == 1          # DEVERR_BAD_INDEX
     assert torch.isfinite(out.float()).all()
     assert L.csa_get_device_status() == 0
+
+
+def test_bounded_wait_reports_timeout_and_recovers():
+    """The device-side timeout path, made to run out on purpose: with the test hook the one-launch
+    decode indexer skips its first cache-tile load and its waits (limited to 2 ms) run out; the
+    kernels return, the error word holds the timeout code and csa_sync_status reports
+    CSA_ERR_DEVICE_TIMEOUT. After a reset, the same step without the hook matches the oracle."""
+    import dataclasses
+    bt, pos = _batch("csa_bf16")
+    c, o = Hn.configs(bt.wl)
+    L = Hn.lib()
+    L.csa_get_device_status(reset=True)
+    L.csa_compress(c, bt.cache(), 0, bt.wl.n_entries)
+    B = bt.B
+    P = torch.from_numpy(pos).cuda()
+    out = torch.zeros((B, c.H, c.d), dtype=c.dtype, device="cuda")
+    topk = torch.full((B, c.top_k), -7, dtype=torch.int32, device="cuda")
+    L.csa_decode(dataclasses.replace(c, test_stall=True), P, bt.cache(), bt.q[:, 0], bt.q_idx[:, 0], bt.w[:, 0],
+                 bt.sink, out, topk)
+    assert L.csa_sync_status() == L.CSA_ERR_DEVICE_TIMEOUT
+    assert L.csa_sync_status() == L.CSA_ERR_DEVICE_TIMEOUT      # the word is kept until reset
+    assert L.csa_get_device_status(reset=True) == 2
+    assert L.csa_sync_status() == 0
+    L.csa_decode(c, P, bt.cache(), bt.q[:, 0], bt.q_idx[:, 0], bt.w[:, 0], bt.sink, out, topk)
+    assert L.csa_sync_status() == 0
+    ckv, cidx = Hn.host64(bt.ckv), Hn.host64(bt.cidx)
+    for b, t in enumerate(pos):
+        t = int(t)
+        sel = topk[b].cpu().numpy()
+        ref_s = O.index_scores(bt.reqs[b]["q_idx"][0], bt.reqs[b]["w"][0], cidx[b], t, c.ratio)
+        Hn.check_topk_vs_oracle(sel, ref_s, c.top_k, f"after the timeout b{b}")
+        ref = O.sparse_attn(bt.reqs[b]["q"][0], bt.reqs[b]["kv"], ckv[b], sel, bt.shared["sink"], t, o)
+        Hn.check_attn(Hn.host64(out[b]), ref, bt.wl.storage, f"after the timeout b{b}")
 
 
 def test_argument_errors_launch_nothing():

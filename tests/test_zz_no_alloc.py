@@ -50,6 +50,50 @@ def test_static_scratch_matches_workspace_call_twice():
     assert L.csa_get_device_status() == 0
 
 
+@pytest.mark.parametrize("case", ["f32_simt", "bf16_multi_query", "bf16_caller_scores_large"])
+def test_static_scratch_other_paths(case):
+    """The other indexer paths that can run without a workspace, twice in a row, against
+    csa_index_topk: the float32 CUDA-core indexer (the tiny workload's shape), several queries per
+    request, and caller-provided scores for a request whose own score buffer would not fit the
+    static array (the scratch then holds only what the call uses)."""
+    L = Hn.lib()
+    rng = np.random.default_rng(len(case))
+    for rep in range(2):
+        if case == "f32_simt":
+            c = L.Config(H=8, H_idx=8, top_k=64, ratio=4, storage="f32")
+            B, S, n_cap, H_idx = 2, 1, 512 - 37 * rep, 8
+        elif case == "bf16_multi_query":
+            c = L.Config(top_k=512, ratio=4)
+            B, S, n_cap, H_idx = 2, 3, 6000 + 1000 * rep, 64
+        else:
+            c = L.Config(top_k=512, ratio=4)
+            B, S, n_cap, H_idx = 2, 80, 16384, 64          # 10.5 MB of scores: beyond the array
+        st = c.storage
+        cidx = rng.standard_normal((B, n_cap, 128), dtype=np.float32) / np.float32(np.sqrt(128))
+        q_idx = rng.standard_normal((B, S, H_idx, 128), dtype=np.float32) / np.float32(np.sqrt(128))
+        if st == "bf16":
+            cidx, q_idx = synth.round_bf16(cidx), synth.round_bf16(q_idx)
+        w = (rng.standard_normal((B, S, H_idx)) / np.sqrt(128 * H_idx)).astype(np.float32)
+        pos = np.stack([4 * n_cap - 1 - 9 * np.arange(S) - 5 * b for b in range(B)]).astype(np.int64)
+        pos_d, q_d, w_d, c_d = (torch.from_numpy(pos).cuda(), Hn.dev(q_idx, st), torch.from_numpy(w).cuda(),
+                                Hn.dev(cidx, st))
+        ref_topk = torch.empty(B, S, c.top_k, dtype=torch.int32, device="cuda")
+        ref_scores = torch.empty(B, S, n_cap, dtype=torch.float32, device="cuda")
+        L.csa_index_topk(c, pos_d, q_d, w_d, c_d, ref_topk, ref_scores)
+        got_topk = torch.full((B, S, c.top_k), -7, dtype=torch.int32, device="cuda")
+        got_scores = torch.full((B, S, n_cap), float("nan"), device="cuda") if case != "f32_simt" else None
+        L.csa_index_topk_static(c, pos_d, q_d, w_d, c_d, got_topk, got_scores)
+        torch.cuda.synchronize()
+        assert torch.equal(got_topk, ref_topk), f"{case} call {rep}: selections differ"
+        if got_scores is not None:
+            for b in range(B):
+                for s_ in range(S):
+                    V = int(pos[b, s_] + 1) // 4
+                    Hn.check_scores(got_scores[b, s_, :V].double().cpu().numpy(),
+                                    ref_scores[b, s_, :V].double().cpu().numpy(), st, f"{case} b{b} s{s_}")
+    assert L.csa_get_device_status() == 0
+
+
 def test_static_scratch_rejects_oversized_request():
     L = Hn.lib()
     c = L.Config(top_k=512, ratio=4)
