@@ -34,16 +34,17 @@ DECODE_WL = synth.WORKLOADS[1]
 PREFILL_WL = synth.WORKLOADS[2]
 ROTATIONS = 3                      # input copies cycled between steps (defeats the 126 MB L2)
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-# DRAM bytes (read + write) of one decode indexer launch at the decode workload, from an ncu capture
-# (profiles/index_tc_decode_B32_N65536.md). They hold only for the kernel source they were taken
-# on: the roofline's "traffic" is null as soon as the code of any of these files differs from
-# that capture.
-INDEX_TRAFFIC = {"bytes_per_launch": 135505920 + 1793024,
-                 "sources": ["long_context_sparse_19_b300/csrc/tc_index.cu",
+# DRAM bytes (read + write) of one launch of the fused decode indexer (scores, closing entries,
+# top-k selection) at the decode workload. Captured on B=4 requests (one kernel, one launch; the
+# profile is profiles/index_select_decode_B32_N65536.md) and scaled by 8 to B=32: every request
+# streams its own cache, so the bytes grow with B. They hold only for the kernel source they were
+# taken on: the roofline's "traffic" is null as soon as the code of any of these files differs.
+INDEX_TRAFFIC = {"bytes_per_launch": 8 * (19147776 + 0),
+                 "sources": ["long_context_sparse_19_b300/csrc/tc_index_select.cu",
                              "long_context_sparse_19_b300/csrc/tc_ptx.cuh",
                              "long_context_sparse_19_b300/csrc/common.cuh",
                              "long_context_sparse_19_b300/csrc/close_entry.cuh"],
-                 "sha256": "44f1dd8972b692fb2d8e71008b68383a0f1f30fdbce5fcbf6141fe2c685850b3"}
+                 "sha256": "92451fddf78a6a50e231624165715d9cfa3e537d47688648ba1ba7fd69d16efa"}
 # GPU sleep queued ahead of each profiled step, so that the host has submitted the whole step before
 # it starts and the per-kernel events time the GPU, not the host's launch rate (~250 us at 2 GHz)
 PROFILE_SLEEP_CYCLES = 500_000
@@ -364,7 +365,7 @@ def run_decode(args, world, rank, device, peaks) -> dict:
         "stage_sum_ms_per_step": sum(v[0] for v in prof.values()) / K,
         "stages_ms_per_step": {k: round(v[0] / K, 5) for k, v in prof.items()},
         "stage_launches": {k: v[1] for k, v in prof.items()},
-        "roofline": {"kernel": "indexer scores (csa_index_topk / csa_decode stage 1)", "bound": "hbm",
+        "roofline": {"kernel": "fused indexer: scores + closing entries + top-k (csa_decode stage 1)", "bound": "hbm",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": (achieved / peaks["hbm_gbs"]) if achieved else None, "traffic": index_traffic(),
                      "algorithmic_bytes_per_launch": work["index_bytes"],
@@ -529,12 +530,13 @@ def time_graph(call, K: int, W: int) -> float:
     return e0.elapsed_time(e1) / K
 
 
-def run_decode_workload(cid: int, args, device, peaks) -> dict:
+def run_decode_workload(cid: int, args, device, peaks, wl: synth.Workload | None = None) -> dict:
     """One decode step of workload `cid` per step (CUDA graph of csa_decode), plus the full-cache
-    compressor build of the same workload and the oracle timed on the host beside it."""
+    compressor build of the same workload and the oracle timed on the host beside it. `wl`
+    overrides the workload's shape (a reduced case, e.g. for a profiler capture)."""
     import torch
     import long_context_sparse_19_b300 as L
-    wl = synth.WORKLOADS[cid]
+    wl = wl or synth.WORKLOADS[cid]
     B = wl.B
     cfg = make_cfg(wl)
     T = device_inputs(wl, list(range(B)), device)
@@ -807,6 +809,12 @@ def main():
     ap.add_argument("--cpu-budget-extra", type=float, default=3.0,
                     help="seconds of oracle work beside each of the other decode workloads")
     ap.add_argument("--no-workloads", action="store_true", help="skip the other decode workloads")
+    ap.add_argument("--workload", type=int, default=None, choices=(0, 1, 3, 4),
+                    help="run only this decode workload's leg (with --wl-B / --wl-N to reduce it) and print it")
+    ap.add_argument("--wl-B", type=int, default=0, help="requests of the --workload leg (default: the workload's)")
+    ap.add_argument("--wl-N", type=int, default=0,
+                    help="raw tokens per request of the --workload leg (default: the workload's; the query "
+                         "sits at the last token)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--B", type=int, default=0, help="requests per GPU (default: the workload's 32)")
@@ -827,6 +835,17 @@ def main():
     world, rank, local = dist_setup()
     device = torch.device("cuda", torch.cuda.current_device())
     peaks = load_peaks()
+    if args.workload is not None:                 # one decode workload, possibly reduced
+        import dataclasses
+        wl = synth.WORKLOADS[args.workload]
+        kw = {}
+        if args.wl_B:
+            kw["B"] = args.wl_B
+        if args.wl_N:
+            kw.update(N=args.wl_N, t=args.wl_N - 1)
+        wl = dataclasses.replace(wl, **kw)
+        print(json.dumps(run_decode_workload(args.workload, args, device, peaks, wl)), flush=True)
+        return
     # the host-side oracle baseline runs first (rank 0, N = 1), before the GPU is busy
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
