@@ -51,7 +51,25 @@ typedef enum {
   CSA_ERR_DEVICE_TIMEOUT = 8   /* a kernel's bounded wait ran out (error word DEVERR 2)     */
 } csa_status;
 
-typedef enum { CSA_F32 = 0, CSA_BF16 = 1 } csa_dtype;
+/* Storage of the compressed caches. CSA_FP4 (the low-precision cache of [LAB41] "Lab tổng hợp
+ * DeepSeek-V4.1-Flash", section "3 Giải pháp": FP4 E2M1 for the latent, FP8 E4M3 for the RoPE tail):
+ * raw rows, q, q_idx and out are bfloat16; ckv and cidx are byte buffers of csa_cache_bytes() bytes
+ * per request laid out as below. Of a compressed entry of C dims (C = d or d_idx), the first
+ * L = C - d_rope dims are E2M1 codes in blocks of 32 dims that share the scale 2^E (E8M0 byte E + 127,
+ * E = floor(log2 max|x|) - 2 clamped to [-127, 127], -127 for an all-zero block; x / 2^E rounded to
+ * nearest even, saturated to +-6: the OCP MXFP4 rule), the last d_rope dims are E4M3 codes (rounded
+ * to nearest even, saturated to +-448). One request's cache of n_cap entries is three planes:
+ *   plane 0, offset 0:                    n_cap x L/2 bytes; byte j of an entry = dims 2j (low
+ *                                          nibble) and 2j+1 (high nibble)
+ *   plane 1, offset n_cap L/2:            n_cap x d_rope bytes of E4M3 codes
+ *   plane 2, offset n_cap (L/2 + d_rope): n_cap x sb bytes, byte k < L/32 = the scale byte of dims
+ *                                          32k .. 32k+31, the rest 0; sb = 16 for C = 512, 2 for C = 128
+ * and requests follow one another at the stride csa_cache_bytes() (304 bytes per KV entry, 98 per
+ * index entry, plus the padding of plane 2 to 16 bytes). The decode calls (S = 1, CSA) read this
+ * format inside their kernels when the one-launch indexer and the fused attention apply (see
+ * csa_decode); every other call that reads a low-precision cache first expands the entries it
+ * reads into bf16 copies in the workspace (csa_workspace_bytes counts them). */
+typedef enum { CSA_F32 = 0, CSA_BF16 = 1, CSA_FP4 = 2 } csa_dtype;
 
 /* csa_config.flags */
 #define CSA_FLAG_SIMT 1u       /* use the CUDA-core kernels even where a tcgen05 kernel exists */
@@ -87,7 +105,8 @@ typedef struct {
  *   idx_k, idx_gate [B, N, d_idx]    storage   raw index keys and their gate logits (NULL for HCA)
  *   idx_bias        [2*ratio, d_idx] float32   (NULL for HCA)
  *   ckv             [B, n_cap, d]    storage   compressed KV cache (entry i rotated at i*ratio)
- *   cidx            [B, n_cap, d_idx] storage  compressed index cache (NULL for HCA)          */
+ *   cidx            [B, n_cap, d_idx] storage  compressed index cache (NULL for HCA)
+ * (with CSA_FP4 storage the raw rows are bfloat16 and ckv / cidx are the byte layout of csa_dtype) */
 typedef struct {
   const void* kv;
   const void* gate;
@@ -117,6 +136,11 @@ csa_status csa_get_device_status(cudaStream_t stream, int reset, int32_t* code);
 /* Synchronises `stream` and returns the device status as csa_get_device_status(stream, 0, NULL)
  * does, leaving the error word as it is. */
 csa_status csa_sync_status(cudaStream_t stream);
+
+/* Bytes of one request's compressed cache of n_cap entries: which = 0 for ckv (d dims), 1 for cidx
+ * (d_idx dims). n_cap * C * 4 for float32, * 2 for bf16, the plane layout of csa_dtype for CSA_FP4.
+ * Returns 0 for an invalid configuration. */
+size_t csa_cache_bytes(const csa_config* cfg, int32_t which, int64_t n_cap);
 
 /* Workspace bytes needed by csa_index_topk / csa_sparse_attn / csa_decode / csa_prefill for
  * B requests, S queries per request and a compressed capacity of n_cap entries. Returns 0 for

@@ -16,13 +16,15 @@ import torch
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcsa.so")
 
-CSA_F32, CSA_BF16 = 0, 1
+CSA_F32, CSA_BF16, CSA_FP4 = 0, 1, 2
+_STORAGE = {"f32": CSA_F32, "bf16": CSA_BF16, "fp4": CSA_FP4}
 CSA_FLAG_SIMT = 1
 CSA_FLAG_TEST_STALL = 1 << 30          # timeout test hook (include/csa.h)
 CSA_ERR_DEVICE, CSA_ERR_DEVICE_TIMEOUT = 6, 8
 
 # the public entry points declared in include/csa.h
 EXPORTS = ("csa_status_string", "csa_last_error", "csa_get_device_status", "csa_sync_status", "csa_workspace_bytes",
+           "csa_cache_bytes",
            "csa_compress", "csa_index_topk", "csa_index_topk_static", "csa_sparse_attn", "csa_decode",
            "csa_prefill",
            "csa_launch_count", "csa_profile_begin", "csa_profile_end")
@@ -65,6 +67,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.csa_get_device_status.argtypes, L.csa_get_device_status.restype = [vp, c_int, POINTER(c_int32)], c_int
     L.csa_sync_status.argtypes, L.csa_sync_status.restype = [vp], c_int
     L.csa_workspace_bytes.argtypes, L.csa_workspace_bytes.restype = [cp, c_int32, c_int32, c_int64], c_size_t
+    L.csa_cache_bytes.argtypes, L.csa_cache_bytes.restype = [cp, c_int32, c_int64], c_size_t
     L.csa_compress.argtypes, L.csa_compress.restype = [cp, c_int32, POINTER(CsaCache), c_int64, c_int64, vp], c_int
     L.csa_index_topk.argtypes = [cp, c_int32, c_int32, vp, vp, vp, vp, c_int64, vp, vp, vp, c_size_t, vp]
     L.csa_index_topk.restype = c_int
@@ -106,18 +109,23 @@ class Config:
     rope_base: float = 10000.0
     softmax_scale: float = 0.0
     rms_eps: float = 1e-6
-    storage: str = "bf16"
+    storage: str = "bf16"              # "bf16", "f32", or "fp4" (FP4 E2M1 + FP8 E4M3 caches, bf16 rows)
     simt: bool = False
     test_stall: bool = False           # the timeout test hook; never set in production
 
     @property
     def dtype(self) -> torch.dtype:
-        return torch.bfloat16 if self.storage == "bf16" else torch.float32
+        """dtype of raw rows, queries and outputs (and of the caches, except with "fp4")."""
+        return torch.float32 if self.storage == "f32" else torch.bfloat16
+
+    @property
+    def lowp(self) -> bool:
+        return self.storage == "fp4"
 
     def c(self) -> CsaConfig:
         return CsaConfig(self.H, self.d, self.d_rope, self.H_idx, self.d_idx, self.ratio, self.top_k,
                          self.window, self.rope_base, self.softmax_scale, self.rms_eps,
-                         CSA_BF16 if self.storage == "bf16" else CSA_F32,
+                         _STORAGE[self.storage],
                          (CSA_FLAG_SIMT if self.simt else 0) | (CSA_FLAG_TEST_STALL if self.test_stall else 0))
 
 
@@ -133,6 +141,33 @@ def _ptr(t, shape=None, dtype=None, name="tensor"):
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
     return t.data_ptr()
+
+
+def csa_cache_bytes(cfg: Config, which: int, n_cap: int) -> int:
+    """Bytes of one request's compressed cache (which = 0: ckv, 1: cidx)."""
+    return int(load().csa_cache_bytes(ctypes.byref(cfg.c()), which, n_cap))
+
+
+def cache_tensor(cfg: Config, B: int, n_cap: int, which: int, device="cuda") -> torch.Tensor:
+    """An uninitialised compressed cache: [B, n_cap, C] of cfg.dtype, or with "fp4" storage
+    [B, csa_cache_bytes] bytes."""
+    if cfg.lowp:
+        return torch.empty((B, csa_cache_bytes(cfg, which, n_cap)), dtype=torch.uint8, device=device)
+    return torch.empty((B, n_cap, cfg.d_idx if which else cfg.d), dtype=cfg.dtype, device=device)
+
+
+def _n_cap(cfg: Config, t, n_cap):
+    if n_cap is not None:
+        return int(n_cap)
+    if cfg.lowp:
+        raise ValueError("n_cap must be given with fp4 caches")
+    return t.shape[1]
+
+
+def _cache_ptr(cfg: Config, t, which: int, B: int, n_cap: int, name: str):
+    if cfg.lowp:
+        return _ptr(t, (B, csa_cache_bytes(cfg, which, n_cap)), torch.uint8, name)
+    return _ptr(t, (B, n_cap, cfg.d_idx if which else cfg.d), cfg.dtype, name)
 
 
 def _stream(stream) -> int:
@@ -151,22 +186,26 @@ class Cache:
     idx_gate: torch.Tensor | None = None
     idx_bias: torch.Tensor | None = None   # [2m, d_idx] float32
     cidx: torch.Tensor | None = None       # [B, n_cap, d_idx]
+    n_cap: int | None = None               # required with fp4 caches ([B, csa_cache_bytes] bytes)
+
+    def capacity(self, cfg: Config) -> int:
+        return _n_cap(cfg, self.ckv, self.n_cap)
 
     def c(self, cfg: Config) -> CsaCache:
         B, N, _ = self.kv.shape
-        n_cap = self.ckv.shape[1]
+        n_cap = self.capacity(cfg)
         dt = cfg.dtype
         m = cfg.ratio
         k = CsaCache()
         k.kv = _ptr(self.kv, (B, N, cfg.d), dt, "kv")
         k.gate = _ptr(self.gate, (B, N, cfg.d), dt, "gate")
         k.gate_bias = _ptr(self.gate_bias, (2 * m, cfg.d), torch.float32, "gate_bias")
-        k.ckv = _ptr(self.ckv, (B, n_cap, cfg.d), dt, "ckv")
+        k.ckv = _cache_ptr(cfg, self.ckv, 0, B, n_cap, "ckv")
         if self.idx_k is not None:
             k.idx_k = _ptr(self.idx_k, (B, N, cfg.d_idx), dt, "idx_k")
             k.idx_gate = _ptr(self.idx_gate, (B, N, cfg.d_idx), dt, "idx_gate")
             k.idx_bias = _ptr(self.idx_bias, (2 * m, cfg.d_idx), torch.float32, "idx_bias")
-            k.cidx = _ptr(self.cidx, (B, n_cap, cfg.d_idx), dt, "cidx")
+            k.cidx = _cache_ptr(cfg, self.cidx, 1, B, n_cap, "cidx")
         k.N, k.n_cap = N, n_cap
         return k
 
@@ -203,39 +242,39 @@ def csa_compress(cfg: Config, cache: Cache, first_entry: int, n_entries: int, st
                                _stream(stream)), "csa_compress")
 
 
-def csa_index_topk(cfg: Config, pos, q_idx, w, cidx, topk, scores=None, ws=None, stream=None) -> None:
+def csa_index_topk(cfg: Config, pos, q_idx, w, cidx, topk, scores=None, ws=None, stream=None, n_cap=None) -> None:
     B, S = pos.shape
-    n_cap = cidx.shape[1]
+    n_cap = _n_cap(cfg, cidx, n_cap)
     ws = workspace(cfg, B, S, n_cap) if ws is None else ws
     _check(load().csa_index_topk(
         ctypes.byref(cfg.c()), B, S, _ptr(pos, (B, S), torch.int64, "pos"),
         _ptr(q_idx, (B, S, cfg.H_idx, cfg.d_idx), cfg.dtype, "q_idx"), _ptr(w, (B, S, cfg.H_idx), torch.float32, "w"),
-        _ptr(cidx, (B, n_cap, cfg.d_idx), cfg.dtype, "cidx"), n_cap,
+        _cache_ptr(cfg, cidx, 1, B, n_cap, "cidx"), n_cap,
         _ptr(topk, (B, S, cfg.top_k), torch.int32, "topk"), _ptr(scores, (B, S, n_cap), torch.float32, "scores"),
         _ptr(ws, None, torch.uint8, "ws"), ws.numel(), _stream(stream)), "csa_index_topk")
 
 
-def csa_index_topk_static(cfg: Config, pos, q_idx, w, cidx, topk, scores=None, stream=None) -> None:
+def csa_index_topk_static(cfg: Config, pos, q_idx, w, cidx, topk, scores=None, stream=None, n_cap=None) -> None:
     """csa_index_topk without a workspace: the library's fixed device scratch array is used instead
     (nothing is allocated; see include/csa.h for the size limit and the sharing rules)."""
     B, S = pos.shape
-    n_cap = cidx.shape[1]
+    n_cap = _n_cap(cfg, cidx, n_cap)
     _check(load().csa_index_topk_static(
         ctypes.byref(cfg.c()), B, S, _ptr(pos, (B, S), torch.int64, "pos"),
         _ptr(q_idx, (B, S, cfg.H_idx, cfg.d_idx), cfg.dtype, "q_idx"), _ptr(w, (B, S, cfg.H_idx), torch.float32, "w"),
-        _ptr(cidx, (B, n_cap, cfg.d_idx), cfg.dtype, "cidx"), n_cap,
+        _cache_ptr(cfg, cidx, 1, B, n_cap, "cidx"), n_cap,
         _ptr(topk, (B, S, cfg.top_k), torch.int32, "topk"), _ptr(scores, (B, S, n_cap), torch.float32, "scores"),
         _stream(stream)), "csa_index_topk_static")
 
 
-def csa_sparse_attn(cfg: Config, pos, q, kv, ckv, topk, sink, out, ws=None, stream=None) -> None:
+def csa_sparse_attn(cfg: Config, pos, q, kv, ckv, topk, sink, out, ws=None, stream=None, n_cap=None) -> None:
     B, S = pos.shape
-    N, n_cap = kv.shape[1], ckv.shape[1]
+    N, n_cap = kv.shape[1], _n_cap(cfg, ckv, n_cap)
     ws = workspace(cfg, B, S, n_cap) if ws is None else ws
     _check(load().csa_sparse_attn(
         ctypes.byref(cfg.c()), B, S, _ptr(pos, (B, S), torch.int64, "pos"),
         _ptr(q, (B, S, cfg.H, cfg.d), cfg.dtype, "q"), _ptr(kv, (B, N, cfg.d), cfg.dtype, "kv"), N,
-        _ptr(ckv, (B, n_cap, cfg.d), cfg.dtype, "ckv"), n_cap,
+        _cache_ptr(cfg, ckv, 0, B, n_cap, "ckv"), n_cap,
         _ptr(topk, (B, S, cfg.top_k), torch.int32, "topk") if cfg.top_k else None,
         _ptr(sink, (cfg.H,), torch.float32, "sink"), _ptr(out, (B, S, cfg.H, cfg.d), cfg.dtype, "out"),
         _ptr(ws, None, torch.uint8, "ws"), ws.numel(), _stream(stream)), "csa_sparse_attn")
@@ -244,7 +283,7 @@ def csa_sparse_attn(cfg: Config, pos, q, kv, ckv, topk, sink, out, ws=None, stre
 def csa_decode(cfg: Config, pos, cache: Cache, q, q_idx, w, sink, out, topk_out=None, ws=None,
                stream=None) -> None:
     B = pos.shape[0]
-    n_cap = cache.ckv.shape[1]
+    n_cap = cache.capacity(cfg)
     ws = workspace(cfg, B, 1, n_cap) if ws is None else ws
     hca = cfg.top_k == 0
     _check(load().csa_decode(
@@ -260,7 +299,7 @@ def csa_decode(cfg: Config, pos, cache: Cache, q, q_idx, w, sink, out, topk_out=
 def csa_prefill(cfg: Config, cache: Cache, q, q_idx, w, sink, out, topk_out=None, ws=None,
                 stream=None) -> None:
     B, S = q.shape[0], q.shape[1]
-    n_cap = cache.ckv.shape[1]
+    n_cap = cache.capacity(cfg)
     ws = workspace(cfg, B, S, n_cap) if ws is None else ws
     hca = cfg.top_k == 0
     _check(load().csa_prefill(
@@ -294,7 +333,7 @@ def bind_decode(cfg: Config, pos, cache: Cache, q, q_idx, w, sink, out, topk_out
     """csa_decode with every argument marshalled once; the returned callable enqueues one decode
     step on the current stream (so it can be replayed or captured into a CUDA graph cheaply)."""
     B = pos.shape[0]
-    n_cap = cache.ckv.shape[1]
+    n_cap = cache.capacity(cfg)
     ws = workspace(cfg, B, 1, n_cap) if ws is None else ws
     hca = cfg.top_k == 0
     c = cfg.c()

@@ -12,6 +12,7 @@
 
 #include "../../include/csa.h"
 #include "kernels.h"
+#include "lowp.cuh"
 #include "tc.h"
 
 namespace {
@@ -90,7 +91,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 csa_status check_config(const csa_config* c) {
   if (!c) return fail(CSA_ERR_INVALID_ARG, "cfg is NULL");
-  if (c->storage != CSA_F32 && c->storage != CSA_BF16) return fail(CSA_ERR_DTYPE, "storage dtype %d", (int)c->storage);
+  if (c->storage != CSA_F32 && c->storage != CSA_BF16 && c->storage != CSA_FP4)
+    return fail(CSA_ERR_DTYPE, "storage dtype %d", (int)c->storage);
   if (c->d != 512) return fail(CSA_ERR_SHAPE, "d = %d (supported: 512)", c->d);
   if (c->d_rope != 64) return fail(CSA_ERR_SHAPE, "d_rope = %d (supported: 64)", c->d_rope);
   if (c->H < 1 || c->H > 64) return fail(CSA_ERR_SHAPE, "H = %d (supported: 1..64)", c->H);
@@ -123,14 +125,27 @@ float softmax_scale(const csa_config* c) {
   return c->softmax_scale > 0.f ? c->softmax_scale : (float)(1.0 / sqrt((double)c->d));
 }
 
+// Low-precision caches (raw rows, queries and outputs in bf16).
+bool lowp(const csa_config* c) { return c->storage == CSA_FP4; }
+// Raw rows, queries and outputs in bf16 (every storage but float32).
+bool bf16_io(const csa_config* c) { return c->storage != CSA_F32; }
+int store_kind(const csa_config* c) {
+  return c->storage == CSA_FP4 ? kStoreLowp : c->storage == CSA_BF16 ? kStoreBf16 : kStoreF32;
+}
+
 bool use_tc_index(const csa_config* c) {
-  return tc_index_available() && c->storage == CSA_BF16 && !(c->flags & CSA_FLAG_SIMT) && c->top_k > 0 &&
-         c->H_idx == 64 && c->d_idx == 128;
+  return tc_index_available() && bf16_io(c) && !(c->flags & CSA_FLAG_SIMT) && c->top_k > 0 && c->H_idx == 64 &&
+         c->d_idx == 128;
 }
 
 bool use_tc_attn(const csa_config* c) {
-  return tc_attn_available() && c->storage == CSA_BF16 && !(c->flags & CSA_FLAG_SIMT) && c->H == 64 &&
-         c->d == 512;
+  return tc_attn_available() && bf16_io(c) && !(c->flags & CSA_FLAG_SIMT) && c->H == 64 && c->d == 512;
+}
+
+// Cluster size of the fused decode indexer + selection for this call, or 0 when it does not apply.
+int fused_select_cluster(const csa_config* c, int B, int S, int64_t n_cap) {
+  if (S != 1 || !use_tc_index(c)) return 0;
+  return tc_index_select_cluster(B, n_cap);
 }
 
 // ------------------------------------------------------------------ launch counting / stage profiling
@@ -190,7 +205,11 @@ struct Plan {
   int fused = 0;                     // decode: cluster size of the fused attention + merge (0: split path)
   int f_wc = 0, f_kc = 0, f_rows = 0;
   int n_split = 1, split_len = 0;
+  // low-precision caches: the one-launch indexer reads cidx directly (idx_direct); otherwise the
+  // entries a call reads are first expanded into bf16 copies in the workspace (dq_idx, dq_kv)
+  bool idx_direct = false, dq_idx = false, dq_kv = false;
   size_t off_scores = 0, off_topk = 0, off_tksel = 0, off_po = 0, off_pml = 0, off_tc = 0, total = 0;
+  size_t off_dq_idx = 0, off_dq_kv = 0;
 };
 
 Plan make_plan(const csa_config* c, int B, int S, int64_t n_cap) {
@@ -233,6 +252,18 @@ Plan make_plan(const csa_config* c, int B, int S, int64_t n_cap) {
   }
   p.off_tc = o;
   o = up(o + tc_workspace_bytes(B, S, n_cap, c->top_k));
+  if (lowp(c)) {
+    if (S == 1 && !hca) {
+      p.idx_direct = fused_select_cluster(c, B, S, n_cap) > 0;
+      p.dq_idx = !p.idx_direct;
+      p.dq_kv = !p.fused;
+    } else {
+      p.dq_idx = !hca;
+      p.dq_kv = true;
+    }
+    if (p.dq_idx) { p.off_dq_idx = o; o = up(o + (size_t)B * (size_t)n_cap * c->d_idx * 2); }
+    if (p.dq_kv) { p.off_dq_kv = o; o = up(o + (size_t)B * (size_t)n_cap * c->d * 2); }
+  }
   p.total = o;
   return p;
 }
@@ -268,14 +299,8 @@ csa_status run_compress(const csa_config* c, int B, const csa_cache* k, int64_t 
   const CompressParams p = compress_params(c, k, first, n, pos);
   // the compressor is the first kernel of every call that runs it: a normal (fully ordered) launch
   return cuda_status(
-      launch_stage(ST_COMPRESS, st, [&] { return launch_compress(c->storage == CSA_BF16, B, p, st, false); }),
+      launch_stage(ST_COMPRESS, st, [&] { return launch_compress(store_kind(c), B, p, st, false); }),
       "compress launch");
-}
-
-// Cluster size of the fused decode indexer + selection for this call, or 0 when it does not apply.
-int fused_select_cluster(const csa_config* c, int B, int S, int64_t n_cap) {
-  if (S != 1 || !use_tc_index(c)) return 0;
-  return tc_index_select_cluster(B, n_cap);
 }
 
 // `scores`: where the scores go; `scores_out`: the caller's score output (nullable), the only
@@ -284,15 +309,15 @@ csa_status run_index_topk(const csa_config* c, int B, int S, const int64_t* pos,
                           const float* w, const void* cidx, int64_t n_cap, int32_t* topk,
                           float* scores, float* scores_out, void* tk_ws, void* tc_ws, cudaStream_t st,
                           bool pdl, const CompressParams* close = nullptr, const void* ckv_prefetch = nullptr) {
-  const bool bf16 = c->storage == CSA_BF16;
-  const int clu = fused_select_cluster(c, B, S, n_cap);
+  const bool bf16 = bf16_io(c);
+  const int clu = fused_select_cluster(c, B, S, n_cap);     // with lowp(c): cidx is the low-precision cache
   if (clu > 0) {
     const RopeTab rope = make_rope(c);
     int32_t* err = device_error_word();
     return cuda_status(launch_stage(ST_INDEX, st, [&] {
                          return tc_index_select(B, clu, pos, q_idx, w, cidx, n_cap, c->ratio, c->top_k, rope,
                                                 scores_out, topk, err, st, pdl, close, ckv_prefetch,
-                                                (c->flags & CSA_FLAG_TEST_STALL) != 0);
+                                                (c->flags & CSA_FLAG_TEST_STALL) != 0, lowp(c));
                        }),
                        "fused indexer + selection launch");
   }
@@ -328,11 +353,12 @@ csa_status run_attn(const csa_config* c, const Plan& pl, int B, int S, const int
   ap.ratio = c->ratio; ap.window = c->window; ap.n_split = pl.n_split; ap.split_len = pl.split_len;
   ap.scale = softmax_scale(c); ap.rope = make_rope(c); ap.err = device_error_word();
   if (pl.n_split > 1 || pl.tc_attn) { ap.part_o = carve<float>(ws, pl.off_po); ap.part_ml = carve<float>(ws, pl.off_pml); }
-  const bool bf16 = c->storage == CSA_BF16;
+  const bool bf16 = bf16_io(c);
   cudaError_t e;
-  if (pl.fused) {
+  if (pl.fused) {                             // with lowp(c): ckv is the low-precision cache
     e = launch_stage(ST_ATTN, st, [&] {
-      return tc_attn_fused(B, pl.fused, pl.f_wc, pl.f_kc, pl.f_rows, ap, carve<char>(ws, pl.off_po), st, pdl);
+      return tc_attn_fused(B, pl.fused, pl.f_wc, pl.f_kc, pl.f_rows, ap, carve<char>(ws, pl.off_po), st, pdl,
+                           lowp(c));
     });
     return cuda_status(e, "fused decode attention launch");
   }
@@ -355,6 +381,17 @@ csa_status check_cache_ptrs(const csa_config* c, const csa_cache* k, bool need_i
   if (k->N < 1 || k->n_cap < 1) return fail(CSA_ERR_SHAPE, "cache N = %lld, n_cap = %lld", (long long)k->N, (long long)k->n_cap);
   (void)c;
   return CSA_OK;
+}
+
+// Low-precision cache -> its bf16 copy in the workspace (entries < n_max, limited to the visible ones
+// of pos[b] when pos is non-null).
+csa_status run_dequant(const csa_config* c, int B, int which, const void* src, int64_t n_cap, int64_t n_max,
+                       const int64_t* pos, void* dst, cudaStream_t st, bool pdl) {
+  const int C = which ? c->d_idx : c->d;
+  return cuda_status(launch_stage(ST_COMPRESS, st, [&] {
+                       return launch_dequant_cache(B, C, c->d_rope, src, n_cap, n_max, pos, c->ratio, dst, st, pdl);
+                     }),
+                     "cache expansion launch");
 }
 
 }  // namespace
@@ -400,6 +437,13 @@ csa_status csa_get_device_status(cudaStream_t stream, int reset, int32_t* code) 
 
 csa_status csa_sync_status(cudaStream_t stream) { return csa_get_device_status(stream, 0, nullptr); }
 
+size_t csa_cache_bytes(const csa_config* cfg, int32_t which, int64_t n_cap) {
+  if (check_config(cfg) != CSA_OK || n_cap < 0 || (which != 0 && which != 1)) return 0;
+  const int C = which ? cfg->d_idx : cfg->d;
+  if (cfg->storage == CSA_FP4) return (size_t)lowp_layout(C, n_cap, cfg->d_rope).stride;
+  return (size_t)n_cap * C * (cfg->storage == CSA_F32 ? 4 : 2);
+}
+
 size_t csa_workspace_bytes(const csa_config* cfg, int32_t B, int32_t S, int64_t n_cap) {
   if (check_config(cfg) != CSA_OK || B < 0 || S < 0 || n_cap < 0) return 0;
   return make_plan(cfg, B, S, n_cap).total;
@@ -436,8 +480,17 @@ csa_status csa_index_topk(const csa_config* cfg, int32_t B, int32_t S, const int
   if (s != CSA_OK) return s;
   if (B == 0 || S == 0) return CSA_OK;
   float* sc = scores ? scores : carve<float>(ws, pl.off_scores);
-  return run_index_topk(cfg, B, S, pos, q_idx, w, cidx, n_cap, topk, sc, scores, carve<char>(ws, pl.off_tksel),
-                        carve<char>(ws, pl.off_tc), stream, false);
+  const void* ci = cidx;
+  bool pdl = false;
+  if (pl.dq_idx) {
+    s = run_dequant(cfg, B, 1, cidx, n_cap, n_cap, S == 1 ? pos : nullptr, carve<char>(ws, pl.off_dq_idx), stream,
+                    false);
+    if (s != CSA_OK) return s;
+    ci = carve<char>(ws, pl.off_dq_idx);
+    pdl = true;
+  }
+  return run_index_topk(cfg, B, S, pos, q_idx, w, ci, n_cap, topk, sc, scores, carve<char>(ws, pl.off_tksel),
+                        carve<char>(ws, pl.off_tc), stream, pdl);
 }
 
 csa_status csa_index_topk_static(const csa_config* cfg, int32_t B, int32_t S, const int64_t* pos,
@@ -452,6 +505,10 @@ csa_status csa_index_topk_static(const csa_config* cfg, int32_t B, int32_t S, co
   // Scratch actually used: nothing on the fused decode path (scores stay on chip); otherwise the
   // float32 scores when the caller passes none, then the candidate lists of long rows.
   const bool fused = fused_select_cluster(cfg, B, S, n_cap) > 0;
+  if (lowp(cfg) && !fused)
+    return fail(CSA_ERR_WORKSPACE,
+                "csa_index_topk_static: a low-precision index cache outside the one-launch decode indexer needs "
+                "a bf16 copy in a workspace; call csa_index_topk with a workspace instead");
   const size_t rows = (size_t)B * (size_t)S;
   const size_t sc_bytes = (fused || scores) ? 0 : up(rows * (size_t)n_cap * sizeof(float));
   const size_t tk_bytes = fused ? 0 : topk_workspace_bytes((int64_t)rows, n_cap, cfg->top_k);
@@ -483,7 +540,16 @@ csa_status csa_sparse_attn(const csa_config* cfg, int32_t B, int32_t S, const in
   s = check_ws(pl, ws, ws_bytes);
   if (s != CSA_OK) return s;
   if (B == 0 || S == 0) return CSA_OK;
-  return run_attn(cfg, pl, B, S, pos, q, kv, N, ckv, n_cap, topk, sink, out, ws, stream, false);
+  const void* ck = ckv;
+  bool pdl = false;
+  if (pl.dq_kv) {
+    s = run_dequant(cfg, B, 0, ckv, n_cap, n_cap, S == 1 ? pos : nullptr, carve<char>(ws, pl.off_dq_kv), stream,
+                    false);
+    if (s != CSA_OK) return s;
+    ck = carve<char>(ws, pl.off_dq_kv);
+    pdl = true;
+  }
+  return run_attn(cfg, pl, B, S, pos, q, kv, N, ck, n_cap, topk, sink, out, ws, stream, pdl);
 }
 
 csa_status csa_decode(const csa_config* cfg, int32_t B, const int64_t* pos, const csa_cache* cache,
@@ -503,24 +569,49 @@ csa_status csa_decode(const csa_config* cfg, int32_t B, const int64_t* pos, cons
   if (B == 0) return CSA_OK;
   // CSA with the tensor-core indexer: the step's first kernel is the indexer, which also pools the
   // entries that t closes (both caches) before the scores need them. Otherwise the compressor's
-  // close kernel runs first.
-  const bool fused_close = !hca && use_tc_index(cfg);
+  // close kernel runs first. With low-precision caches the indexer pools them only when it is the
+  // one-launch kernel that reads the low-precision index cache itself; every cache that a later
+  // kernel cannot read directly is then expanded into its bf16 copy (the visible entries only).
+  const bool fused_close = !hca && use_tc_index(cfg) && (!lowp(cfg) || pl.idx_direct);
   const CompressParams close = compress_params(cfg, cache, 0, 0, pos);
+  bool after_first = false;
   if (!fused_close) {
     s = run_compress(cfg, B, cache, 0, 0, pos, stream);
     if (s != CSA_OK) return s;
+    after_first = true;
+  }
+  const void* ci = cache->cidx;
+  const void* ck = cache->ckv;
+  if (pl.dq_idx) {
+    s = run_dequant(cfg, B, 1, cache->cidx, cache->n_cap, cache->n_cap, pos, carve<char>(ws, pl.off_dq_idx), stream,
+                    after_first);
+    if (s != CSA_OK) return s;
+    ci = carve<char>(ws, pl.off_dq_idx);
+    after_first = true;
+  }
+  if (pl.dq_kv && hca) {                      // with CSA the KV copy waits for the indexer's close
+    s = run_dequant(cfg, B, 0, cache->ckv, cache->n_cap, cache->n_cap, pos, carve<char>(ws, pl.off_dq_kv), stream,
+                    after_first);
+    if (s != CSA_OK) return s;
+    ck = carve<char>(ws, pl.off_dq_kv);
+    after_first = true;
   }
   int32_t* tk = nullptr;
   if (!hca) {
     tk = topk_out ? topk_out : carve<int32_t>(ws, pl.off_topk);
-    s = run_index_topk(cfg, B, 1, pos, q_idx, w, cache->cidx, cache->n_cap, tk,
+    s = run_index_topk(cfg, B, 1, pos, q_idx, w, ci, cache->n_cap, tk,
                        carve<float>(ws, pl.off_scores), nullptr, carve<char>(ws, pl.off_tksel),
-                       carve<char>(ws, pl.off_tc), stream, !fused_close, fused_close ? &close : nullptr,
+                       carve<char>(ws, pl.off_tc), stream, after_first, fused_close ? &close : nullptr,
                        pl.fused ? cache->ckv : nullptr);
     if (s != CSA_OK) return s;
+    if (pl.dq_kv) {
+      s = run_dequant(cfg, B, 0, cache->ckv, cache->n_cap, cache->n_cap, pos, carve<char>(ws, pl.off_dq_kv), stream,
+                      true);
+      if (s != CSA_OK) return s;
+      ck = carve<char>(ws, pl.off_dq_kv);
+    }
   }
-  return run_attn(cfg, pl, B, 1, pos, q, cache->kv, cache->N, cache->ckv, cache->n_cap, tk, sink, out, ws,
-                  stream, true);
+  return run_attn(cfg, pl, B, 1, pos, q, cache->kv, cache->N, ck, cache->n_cap, tk, sink, out, ws, stream, true);
 }
 
 csa_status csa_prefill(const csa_config* cfg, int32_t B, int32_t S, const csa_cache* cache, const void* q,
@@ -542,15 +633,29 @@ csa_status csa_prefill(const csa_config* cfg, int32_t B, int32_t S, const csa_ca
   if (B == 0 || S == 0) return CSA_OK;
   s = run_compress(cfg, B, cache, 0, S / cfg->ratio, nullptr, stream);
   if (s != CSA_OK) return s;
+  const void* ci = cache->cidx;
+  const void* ck = cache->ckv;
+  if (pl.dq_idx) {                            // low-precision caches: bf16 copies of the S / ratio entries
+    s = run_dequant(cfg, B, 1, cache->cidx, cache->n_cap, S / cfg->ratio, nullptr, carve<char>(ws, pl.off_dq_idx),
+                    stream, true);
+    if (s != CSA_OK) return s;
+    ci = carve<char>(ws, pl.off_dq_idx);
+  }
+  if (pl.dq_kv) {
+    s = run_dequant(cfg, B, 0, cache->ckv, cache->n_cap, S / cfg->ratio, nullptr, carve<char>(ws, pl.off_dq_kv),
+                    stream, true);
+    if (s != CSA_OK) return s;
+    ck = carve<char>(ws, pl.off_dq_kv);
+  }
   int32_t* tk = nullptr;
   if (!hca) {
     tk = topk_out ? topk_out : carve<int32_t>(ws, pl.off_topk);
-    s = run_index_topk(cfg, B, S, nullptr, q_idx, w, cache->cidx, cache->n_cap, tk,
+    s = run_index_topk(cfg, B, S, nullptr, q_idx, w, ci, cache->n_cap, tk,
                        carve<float>(ws, pl.off_scores), nullptr, carve<char>(ws, pl.off_tksel),
                        carve<char>(ws, pl.off_tc), stream, true);
     if (s != CSA_OK) return s;
   }
-  return run_attn(cfg, pl, B, S, nullptr, q, cache->kv, cache->N, cache->ckv, cache->n_cap, tk, sink, out,
+  return run_attn(cfg, pl, B, S, nullptr, q, cache->kv, cache->N, ck, cache->n_cap, tk, sink, out,
                   ws, stream, true);
 }
 

@@ -6,10 +6,12 @@
 // gate + bias row (a token before position 0 takes weight 0), then RMSNorm over the C channels,
 // then RoPE of the last d_rope channels at position e*m. Same arithmetic as the compressor's
 // close kernel (one online-softmax state per channel, tokens in order), with the 2m tokens'
-// loads issued before any is used. bf16 caches only (the tensor-core indexer's storage).
+// loads issued before any is used. bf16 raw rows; the entry is stored as bf16 or, with kLowp, in the
+// low-precision cache format of lowp.cuh.
 #pragma once
 
 #include "kernels.h"
+#include "lowp.cuh"
 
 namespace csa {
 
@@ -47,7 +49,7 @@ __device__ __forceinline__ void load_row_part(const float* p, float (&v)[P]) {
 // Pools entry e of request b of `job` (C channels, bf16 rows) and stores it. Called by all kT
 // threads `tid` = 0..kT-1 of one group (whole warps), which synchronise on named barrier `bar_id`;
 // `red` is kT / 32 floats of shared memory. Returns after this thread's part of the entry is stored.
-template <int C, int kT = 128>
+template <int C, int kT = 128, bool kLowp = false>
 __device__ __forceinline__ void close_entry_bf16(const CompressJob& job, int64_t N, int64_t n_cap, int m,
                                                  float eps, const RopeTab& rope, int64_t b, int64_t e, int tid,
                                                  float* red, int bar_id) {
@@ -114,7 +116,12 @@ __device__ __forceinline__ void close_entry_bf16(const CompressJob& job, int64_t
       rope_cs(e * m, rope, (c0 - r0) / 2, cs, sn);
       x[0] = (c0 & 1) ? fmaf(xp, sn, x[0] * cs) : fmaf(-xp, sn, x[0] * cs);
     }
-    static_cast<__nv_bfloat16*>(job.dst)[(b * n_cap + e) * C + c0] = __float2bfloat16_rn(x[0]);
+    if constexpr (kLowp) {
+      const LowpLayout lay = lowp_layout(C, n_cap, rope.d_rope);
+      store_entry_lowp<1>(static_cast<uint8_t*>(job.dst) + b * lay.stride, lay, e, c0, x);
+    } else {
+      static_cast<__nv_bfloat16*>(job.dst)[(b * n_cap + e) * C + c0] = __float2bfloat16_rn(x[0]);
+    }
   } else {
     if (c0 >= r0) {
 #pragma unroll
@@ -125,6 +132,11 @@ __device__ __forceinline__ void close_entry_bf16(const CompressJob& job, int64_t
         x[2 * q] = a * cs - bb * sn;
         x[2 * q + 1] = a * sn + bb * cs;
       }
+    }
+    if constexpr (kLowp) {
+      const LowpLayout lay = lowp_layout(C, n_cap, rope.d_rope);
+      store_entry_lowp<P>(static_cast<uint8_t*>(job.dst) + b * lay.stride, lay, e, c0, x);
+      return;
     }
     __nv_bfloat16* d = static_cast<__nv_bfloat16*>(job.dst) + (b * n_cap + e) * C + c0;
     if constexpr (P == 2) {

@@ -10,7 +10,10 @@
 // Each raw group g is read ONCE: its tokens update two online-softmax states at the same time,
 // one with the second-half bias rows (for entry g) and one with the first-half bias rows (for
 // entry g+1). An entry is the merge of the two states, which are exact softmax partials.
+// With the low-precision cache (kLowp) the raw rows are bf16 and each finished entry is stored as
+// FP4 E2M1 latent blocks + an FP8 E4M3 tail (lowp.cuh).
 #include "kernels.h"
+#include "lowp.cuh"
 
 namespace csa {
 namespace {
@@ -58,7 +61,7 @@ __device__ __forceinline__ void scan_group(const T* src, const T* gate, const fl
   }
 }
 
-template <typename T, int C>
+template <typename T, int C, bool kLowp>
 __device__ void compress_run(const CompressParams& p, const CompressJob& job, int b, int64_t e_begin,
                              int64_t e_end, int team, int tt, float* red) {
   constexpr int TPE = C / 8;               // threads per entry team
@@ -68,6 +71,10 @@ __device__ void compress_run(const CompressParams& p, const CompressJob& job, in
   const T* gate = reinterpret_cast<const T*>(job.gate) + (int64_t)b * p.N * C;
   T* dst = reinterpret_cast<T*>(job.dst) + (int64_t)b * p.n_cap * C;
   const int lane = threadIdx.x & 31;
+  const LowpLayout lay = lowp_layout(C, p.n_cap, p.rope.d_rope);
+  uint8_t* lbase = static_cast<uint8_t*>(job.dst) + (int64_t)b * lay.stride;
+  // lanes of this team inside the warp (teams narrower than a warp share it)
+  const unsigned tmask = TPE >= 32 ? 0xffffffffu : ((1u << (TPE & 31)) - 1u) << (lane & ~(TPE - 1));
 
   Stat8 prev, lo, hi;
   prev.clear();
@@ -121,11 +128,12 @@ __device__ void compress_run(const CompressParams& p, const CompressJob& job, in
         x[2 * q + 1] = a * s + bq * c;
       }
     }
-    store8(dst + e * C + c0, x);
+    if constexpr (kLowp) store_entry_lowp<8>(lbase, lay, e, c0, x, tmask);
+    else store8(dst + e * C + c0, x);
   }
 }
 
-template <typename T, int C>
+template <typename T, int C, bool kLowp>
 __device__ void compress_block(const CompressParams& p, const CompressJob& job, float* red) {
   constexpr int TPE = C / 8;
   constexpr int TEAMS = kThreads / TPE;
@@ -136,17 +144,17 @@ __device__ void compress_block(const CompressParams& p, const CompressJob& job, 
   const int64_t e_begin = p.first_entry + (int64_t)blockIdx.x * p.epb + (int64_t)team * EPT;
   const int64_t e_end = min(e_begin + EPT, p.first_entry + p.n_entries);
   if (e_begin >= e_end) return;
-  compress_run<T, C>(p, job, b, e_begin, e_end, team, tt, red);
+  compress_run<T, C, kLowp>(p, job, b, e_begin, e_end, team, tt, red);
 }
 
-template <typename T>
+template <typename T, bool kLowp>
 __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressParams p) {
   __shared__ float red[16];
   griddep_launch();
   griddep_wait();
   const CompressJob& job = p.job[blockIdx.z];
-  if (job.C == 512) compress_block<T, 512>(p, job, red);
-  else compress_block<T, 128>(p, job, red);
+  if (job.C == 512) compress_block<T, 512, kLowp>(p, job, red);
+  else compress_block<T, 128, kLowp>(p, job, red);
 }
 
 // ------------------------------------------------------------------ decode: the closing entry only
@@ -156,7 +164,7 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressParams
 // states per channel are then merged in shared memory, one thread per channel.
 constexpr int kCloseThreads = 512;
 
-template <typename T, int C>
+template <typename T, int C, bool kLowp>
 __device__ void compress_close(const CompressParams& p, const CompressJob& job, float* sm) {
   constexpr int CH = C / 8;                  // channel chunks
   constexpr int G = kCloseThreads / CH;      // token groups
@@ -246,44 +254,40 @@ __device__ void compress_close(const CompressParams& p, const CompressJob& job, 
         x[2 * q + 1] = a * sn + bq * cs;
       }
     }
-    T* dst = reinterpret_cast<T*>(job.dst) + ((int64_t)b * p.n_cap + e) * C;
-    store8(dst + c0, x);
+    if constexpr (kLowp) {
+      const LowpLayout lay = lowp_layout(C, p.n_cap, p.rope.d_rope);
+      store_entry_lowp<8>(static_cast<uint8_t*>(job.dst) + (int64_t)b * lay.stride, lay, e, c0, x,
+                          CH >= 32 ? 0xffffffffu : (1u << CH) - 1u);
+    } else {
+      T* dst = reinterpret_cast<T*>(job.dst) + ((int64_t)b * p.n_cap + e) * C;
+      store8(dst + c0, x);
+    }
   }
 }
 
-template <typename T>
+template <typename T, bool kLowp>
 __global__ void __launch_bounds__(kCloseThreads) compress_close_kernel(const CompressParams p) {
   extern __shared__ float sm[];
   if (threadIdx.x == 0) CSA_STAMP(40);
   griddep_launch();
   griddep_wait();
   const CompressJob& job = p.job[blockIdx.y];
-  if (job.C == 512) compress_close<T, 512>(p, job, sm);
-  else compress_close<T, 128>(p, job, sm);
+  if (job.C == 512) compress_close<T, 512, kLowp>(p, job, sm);
+  else compress_close<T, 128, kLowp>(p, job, sm);
   if (threadIdx.x == 0) CSA_STAMP(41);
 }
 
-}  // namespace
-
-cudaError_t launch_compress(bool bf16, int B, const CompressParams& p, cudaStream_t st, bool pdl) {
-  if (B == 0) return cudaSuccess;
+template <typename T, bool kLowp>
+cudaError_t launch_compress_t(int B, const CompressParams& p, cudaStream_t st, bool pdl) {
   if (p.pos) {
     // shared memory: 3 partial states x (token groups x channels), which is kCloseThreads * 8 for
     // both caches, plus the pooled row and reduction scratch
     const size_t smem = (size_t)(3 * kCloseThreads * 8 + 512 + 32) * sizeof(float);
     dim3 grid((unsigned)B, (unsigned)p.n_jobs);
-    cudaError_t e;
-    if (bf16) {
-      e = cudaFuncSetAttribute(compress_close_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
-      if (e != cudaSuccess) return e;
-      e = launch_kernel(pdl, compress_close_kernel<__nv_bfloat16>, grid, dim3(kCloseThreads), smem, st, p);
-    } else {
-      e = cudaFuncSetAttribute(compress_close_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      e = launch_kernel(pdl, compress_close_kernel<float>, grid, dim3(kCloseThreads), smem, st, p);
-    }
-    return e;
+    cudaError_t e = cudaFuncSetAttribute(compress_close_kernel<T, kLowp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(pdl, compress_close_kernel<T, kLowp>, grid, dim3(kCloseThreads), smem, st, p);
   }
   CompressParams q = p;
   q.epb = kEntriesPerBlock;
@@ -291,8 +295,62 @@ cudaError_t launch_compress(bool bf16, int B, const CompressParams& p, cudaStrea
   const int64_t nb = (p.n_entries + q.epb - 1) / q.epb;
   if (nb == 0) return cudaSuccess;
   dim3 grid((unsigned)nb, (unsigned)B, (unsigned)p.n_jobs);
-  if (bf16) return launch_kernel(pdl, compress_kernel<__nv_bfloat16>, grid, dim3(kThreads), 0, st, q);
-  return launch_kernel(pdl, compress_kernel<float>, grid, dim3(kThreads), 0, st, q);
+  return launch_kernel(pdl, compress_kernel<T, kLowp>, grid, dim3(kThreads), 0, st, q);
+}
+
+// ------------------------------------------------------------------ low-precision cache -> bf16
+// One thread per (entry, 8 dims): 4 bytes of E2M1 codes and their block's scale byte, or 8 bytes of
+// E4M3 codes, become one 16-byte bf16 store (exact: every E2M1 value times a power of two and every
+// E4M3 value is a bf16 value).
+__global__ void __launch_bounds__(256) dequant_cache_kernel(const uint8_t* src, int C, int d_rope, int64_t n_cap,
+                                                            int64_t n_max, const int64_t* pos, int ratio,
+                                                            __nv_bfloat16* dst) {
+  griddep_launch();
+  griddep_wait();
+  const int b = blockIdx.y;
+  const LowpLayout lay = lowp_layout(C, n_cap, d_rope);
+  int64_t n = min(n_cap, n_max);
+  if (pos) {
+    const int64_t t = pos[b];
+    n = t < 0 ? 0 : min(n, (t + 1) / ratio);
+  }
+  const int cpe = C / 8;
+  const int64_t total = n * cpe;
+  const uint8_t* base = src + (int64_t)b * lay.stride;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < total; u += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = u / cpe;
+    const int c0 = (int)(u % cpe) * 8;
+    uint4 o;
+    if (c0 < lay.L) {
+      const uint32_t codes = __ldg(reinterpret_cast<const uint32_t*>(base + e * (lay.L / 2) + c0 / 2));
+      o = dequant_fp4x8(codes, e8m0_to_f32(__ldg(base + lay.scale + e * lay.sb + c0 / 32)));
+    } else {
+      const uint2 c = __ldg(reinterpret_cast<const uint2*>(base + lay.fp8 + e * lay.R + (c0 - lay.L)));
+      o = dequant_fp8x8(c.x, c.y);
+    }
+    *reinterpret_cast<uint4*>(dst + ((int64_t)b * n_cap + e) * C + c0) = o;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dequant_cache(int B, int C, int d_rope, const void* src, int64_t n_cap, int64_t n_max,
+                                 const int64_t* pos, int ratio, void* dst, cudaStream_t st, bool pdl) {
+  if (n_max > n_cap) n_max = n_cap;
+  if (B == 0 || n_max <= 0) return cudaSuccess;
+  const int64_t units = n_max * (C / 8);
+  int64_t blocks = (units + 255) / 256;
+  if (blocks > 148 * 8) blocks = 148 * 8;
+  dim3 grid((unsigned)blocks, (unsigned)B);
+  return launch_kernel(pdl, dequant_cache_kernel, grid, dim3(256), 0, st, static_cast<const uint8_t*>(src), C,
+                       d_rope, n_cap, n_max, pos, ratio, static_cast<__nv_bfloat16*>(dst));
+}
+
+cudaError_t launch_compress(int kind, int B, const CompressParams& p, cudaStream_t st, bool pdl) {
+  if (B == 0) return cudaSuccess;
+  if (kind == kStoreLowp) return launch_compress_t<__nv_bfloat16, true>(B, p, st, pdl);
+  if (kind == kStoreBf16) return launch_compress_t<__nv_bfloat16, false>(B, p, st, pdl);
+  return launch_compress_t<float, false>(B, p, st, pdl);
 }
 
 }  // namespace csa

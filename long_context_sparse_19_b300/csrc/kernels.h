@@ -27,8 +27,18 @@ struct CompressParams {
   int32_t* err;
 };
 
+// Storage of the compressed caches: float32, bf16, or the low-precision format of lowp.cuh (FP4 E2M1
+// latent + FP8 E4M3 tail, raw rows in bf16).
+enum StoreKind { kStoreF32 = 0, kStoreBf16 = 1, kStoreLowp = 2 };
+
 // `pdl`: launch as a programmatic dependent of the previous kernel in the stream.
-cudaError_t launch_compress(bool bf16, int B, const CompressParams& p, cudaStream_t st, bool pdl);
+cudaError_t launch_compress(int kind, int B, const CompressParams& p, cudaStream_t st, bool pdl);
+
+// Low-precision caches -> bf16 [B, n_cap, C] copies of entries [0, n) of every request, n =
+// min(n_cap, n_max), further limited to (pos[b] + 1) / ratio when pos is non-null (one position per
+// request).
+cudaError_t launch_dequant_cache(int B, int C, int d_rope, const void* src, int64_t n_cap, int64_t n_max,
+                                 const int64_t* pos, int ratio, void* dst, cudaStream_t st, bool pdl);
 
 // ------------------------------------------------------------------ K2 / K6 indexer scores (SIMT)
 struct IndexParams {

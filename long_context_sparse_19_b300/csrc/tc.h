@@ -31,13 +31,14 @@ cudaError_t tc_index_scores(int B, int S, const int64_t* pos, const void* q_idx,
 // entries and selects the top_k (ascending entry index, -1 padded) into topk [B, top_k]; scores
 // [B, n_cap] is written only when non-null. `close`: as for tc_index_scores. `ckv_prefetch`
 // (nullable): the compressed KV cache, whose selected rows are requested into L2 once selected.
-// `test_stall`: the timeout test hook (csa.h, CSA_FLAG_TEST_STALL).
+// `test_stall`: the timeout test hook (csa.h, CSA_FLAG_TEST_STALL). `lowp`: cidx (and ckv_prefetch, and
+// the entries the close step writes) are in the low-precision format of lowp.cuh.
 // tc_index_select_cluster gives C for B requests of capacity n_cap, or 0 when the kernel does not apply.
 int tc_index_select_cluster(int B, int64_t n_cap);
 cudaError_t tc_index_select(int B, int C, const int64_t* pos, const void* q_idx, const float* w, const void* cidx,
                             int64_t n_cap, int ratio, int top_k, const RopeTab& rope, float* scores, int32_t* topk,
                             int32_t* err, cudaStream_t st, bool pdl, const CompressParams* close = nullptr,
-                            const void* ckv_prefetch = nullptr, bool test_stall = false);
+                            const void* ckv_prefetch = nullptr, bool test_stall = false, bool lowp = false);
 
 // Many-query attention (prefill): one CTA per query over all of its candidates (at most
 // tc_attn_prefill_max_tiles() tiles of 128), final output written directly.
@@ -51,8 +52,9 @@ cudaError_t tc_attn_prefill(int B, const AttnParams& p, cudaStream_t st, bool pd
 // The kernel exchanges its partials through `ws` (tc_attn_fused_workspace bytes).
 int tc_attn_fused_plan(int B, int window, int top_k, int* Wc, int* Kc, int* R);
 size_t tc_attn_fused_workspace(int B, int C);
+// `lowp`: p.ckv is in the low-precision format of lowp.cuh (raw rows, q and out stay bf16).
 cudaError_t tc_attn_fused(int B, int C, int Wc, int Kc, int R, const AttnParams& p, void* ws, cudaStream_t st,
-                          bool pdl);
+                          bool pdl, bool lowp = false);
 
 // Sparse attention (split partials when p.n_split > 1, else the final output).
 cudaError_t tc_sparse_attn(int B, const AttnParams& p, void* ws, cudaStream_t st, bool pdl);

@@ -28,12 +28,16 @@
 // under programmatic dependent launch they are fetched (and rotated) before the kernel waits for
 // the selection kernel. The code on this path runs once per CTA, where instruction fetch
 // dominates, so it is kept to short loops.
+// With the low-precision cache (FP4 E2M1 latent + FP8 E4M3 tail, lowp.cuh; 304 instead of 1024
+// bytes per entry) the selected rows are loaded into registers piece by piece (a 16-byte E2M1 piece
+// is one 32-dim block, read with its scale byte) and expanded into the same bf16 tile (exact).
 // Warps: 0 = Q TMA and tcgen05.mma issuer (one lane), 1..7 gather the window rows, 1 = TMEM owner
 // and RoPE of the query, 2..7 gather the selected rows, 4..7 then run the softmax and the O
 // epilogue (lanes 0..15: one head each, TMEM lane quadrant = warp % 4); all eight merge.
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
+#include "lowp.cuh"
 #include "tc.h"
 #include "tc_ptx.cuh"
 
@@ -63,7 +67,7 @@ static_assert(kMaxRows <= 3 * 64 && 3 * kPBlock + kCluMax * kH * 4 <= kQBytes, "
 
 struct FusedParams {
   const __nv_bfloat16* kv;   // [B, N, 512] raw rows
-  const __nv_bfloat16* ckv;  // [B, n_cap, 512]
+  const void* ckv;           // [B, n_cap, 512] bf16, or the low-precision planes (kLowp)
   const int32_t* topk;       // [B, k]
   const int64_t* pos;        // [B]
   const float* sink;         // [64]
@@ -125,6 +129,7 @@ __device__ __forceinline__ void merge_slice(const FusedParams& p, const float* w
   }
 }
 
+template <bool kLowp>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fused_kernel(const __grid_constant__ CUtensorMap qmap, const FusedParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -198,6 +203,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
     }
     cp_async_commit();
+  };
+
+  // kLowp: rows [r0, r1) from the low-precision cache, 18 pieces a row (14 E2M1 pieces of one 32-dim
+  // block each, 4 E4M3 pieces of 16 dims); a batch of pieces is loaded before any is expanded. Empty
+  // rows read as zero codes, which expand to zeros.
+  auto gather_lowp = [&](int r0, int r1, int g, int ng) {
+    constexpr int kPieces = 18, kBatch = 12;
+    const LowpLayout kl = lowp_layout(kD, p.n_cap, 64);
+    const uint8_t* kb = static_cast<const uint8_t*>(p.ckv) + (int64_t)b * kl.stride;
+    const int n_units = (r1 - r0) * kPieces;
+#pragma unroll 1
+    for (int u0 = g; u0 < n_units; u0 += ng * kBatch) {
+      uint4 v[kBatch];
+      uint32_t sb[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int u = u0 + j * ng;
+        v[j] = make_uint4(0, 0, 0, 0);
+        sb[j] = 0;
+        const int32_t gr = u < n_units ? rows_s[r0 + u / kPieces] : -1;
+        if (gr >= 0) {
+          const int64_t e = gr - (int64_t)b * p.n_cap;
+          const int pc = u % kPieces;
+          if (pc < 14) {
+            v[j] = __ldcg(reinterpret_cast<const uint4*>(kb + e * 224 + pc * 16));
+            sb[j] = kb[kl.scale + e * 16 + pc];
+          } else {
+            v[j] = __ldcg(reinterpret_cast<const uint4*>(kb + kl.fp8 + e * 64 + (pc - 14) * 16));
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int u = u0 + j * ng;
+        if (u >= n_units) continue;
+        const int rr = r0 + u / kPieces, pc = u % kPieces;
+        if (pc < 14) {                                         // dims 32 pc .. 32 pc + 31
+          const float sc = e8m0_to_f32(sb[j]);
+          uint8_t* dst = kvs + (pc >> 1) * kBlkStride;
+          const int c0 = (pc & 1) * 4;
+          *reinterpret_cast<uint4*>(dst + sw128_offset(rr, c0 + 0)) = dequant_fp4x8(v[j].x, sc);
+          *reinterpret_cast<uint4*>(dst + sw128_offset(rr, c0 + 1)) = dequant_fp4x8(v[j].y, sc);
+          *reinterpret_cast<uint4*>(dst + sw128_offset(rr, c0 + 2)) = dequant_fp4x8(v[j].z, sc);
+          *reinterpret_cast<uint4*>(dst + sw128_offset(rr, c0 + 3)) = dequant_fp4x8(v[j].w, sc);
+        } else {                                               // dims 448 + 16 q .. + 15
+          const int q = pc - 14;
+          uint8_t* dst = kvs + 7 * kBlkStride;
+          *reinterpret_cast<uint4*>(dst + sw128_offset(rr, 2 * q)) = dequant_fp8x8(v[j].x, v[j].y);
+          *reinterpret_cast<uint4*>(dst + sw128_offset(rr, 2 * q + 1)) = dequant_fp8x8(v[j].z, v[j].w);
+        }
+      }
+    }
   };
 
   if (warp == 0) {
@@ -288,10 +345,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         rows_s[p.Wc + i] = idx >= 0 && !bad_pos ? (int32_t)((int64_t)b * p.n_cap + idx) : -1;
       }
       named_barrier(2, kGather);                               // the row table is complete
-      gather(p.Wc, R, p.ckv, gs, kGather);
-      cp_async_wait<1>();                                      // this thread's window pieces landed
-      rotate_own_window_pieces();
-      cp_async_wait<0>();
+      if constexpr (kLowp) {
+        gather_lowp(p.Wc, R, gs, kGather);
+        cp_async_wait<0>();                                    // this thread's window pieces landed
+        rotate_own_window_pieces();
+      } else {
+        gather(p.Wc, R, static_cast<const __nv_bfloat16*>(p.ckv), gs, kGather);
+        cp_async_wait<1>();                                    // this thread's window pieces landed
+        rotate_own_window_pieces();
+        cp_async_wait<0>();
+      }
       fence_proxy_async_smem();
       mbar_arrive(bar_kv);
       if (gs == 0) CSA_STAMP(2);
@@ -449,8 +512,10 @@ int tc_attn_fused_plan(int B, int window, int top_k, int* Wc, int* Kc, int* R) {
   *R = ((*Wc + *Kc + 15) / 16) * 16;
   static int fits[kCluMax + 1] = {0};                          // 1 = placeable, -1 = not
   if (!fits[c]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(attn_fused_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_fused_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     int n = 0;
     if (e == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
@@ -464,7 +529,7 @@ int tc_attn_fused_plan(int B, int window, int top_k, int* Wc, int* Kc, int* R) {
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      e = cudaOccupancyMaxActiveClusters(&n, attn_fused_kernel, &cfg);
+      e = cudaOccupancyMaxActiveClusters(&n, attn_fused_kernel<false>, &cfg);
     }
     if (e != cudaSuccess) (void)cudaGetLastError();
     fits[c] = (e == cudaSuccess && n > 0) ? 1 : -1;
@@ -477,19 +542,20 @@ size_t tc_attn_fused_workspace(int B, int C) {
 }
 
 cudaError_t tc_attn_fused(int B, int C, int Wc, int Kc, int R, const AttnParams& a, void* ws, cudaStream_t st,
-                          bool pdl) {
+                          bool pdl, bool lowp) {
   if ((C != 2 && C != 4 && C != 8) || R > kMaxRows || R % 16 != 0 || Wc + Kc > R || a.S != 1 || !a.topk ||
       a.H != kH || !ws)
     return cudaErrorInvalidValue;
   if ((int64_t)B * a.N >= (int64_t)1 << 31 || (int64_t)B * a.n_cap >= (int64_t)1 << 31) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(lowp ? attn_fused_kernel<true> : attn_fused_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   CUtensorMap qmap;
   e = make_tmap_2d(&qmap, a.q, (int64_t)B * kH, kD, kH);
   if (e != cudaSuccess) return e;
   FusedParams p;
   p.kv = static_cast<const __nv_bfloat16*>(a.kv);
-  p.ckv = static_cast<const __nv_bfloat16*>(a.ckv);
+  p.ckv = a.ckv;
   p.topk = a.topk; p.pos = a.pos; p.sink = a.sink; p.out = static_cast<__nv_bfloat16*>(a.out);
   p.part = static_cast<__half*>(ws);
   p.pstat = reinterpret_cast<float*>(static_cast<char*>(ws) + (size_t)B * C * kH * kD * sizeof(__half));
@@ -513,7 +579,7 @@ cudaError_t tc_attn_fused(int B, int C, int Wc, int Kc, int R, const AttnParams&
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, attn_fused_kernel, qmap, p);
+  return cudaLaunchKernelEx(&cfg, lowp ? attn_fused_kernel<true> : attn_fused_kernel<false>, qmap, p);
 }
 
 }  // namespace csa

@@ -31,11 +31,19 @@
 // streams, pool the new index entry in the CTA that scores the request's last tile (its TMA load
 // waits for it) and the new KV entry in CTA 0 (the attention reads it later).
 //
+// With the low-precision cache (FP4 E2M1 dims 0..63 with two block scales, FP8 E4M3 dims 64..127;
+// lowp.cuh) a tile is three bulk copies (4 KB + 8 KB + 256 B of the cache's planes) into a staging
+// ring, and the epilogue warps first expand tile i into the bf16 operand (exact) before they reduce
+// tile i-1: the MMA sees the same operand layout as with a bf16 cache, from 98 instead of 256 bytes
+// per entry.
+//
 // Warps: 0 = TMA producer, 1 = TMEM owner and MMA issuer, 2..5 = query operand and score epilogue
-// (TMEM lane quadrant = warp % 4), 6..7 = close step; all eight select.
+// (TMEM lane quadrant = warp % 4; with the low-precision cache also the expansion of each tile),
+// 6..7 = close step; all eight select.
 #include <cudaTypedefs.h>
 
 #include "close_entry.cuh"
+#include "lowp.cuh"
 #include "tc.h"
 #include "tc_ptx.cuh"
 
@@ -58,6 +66,12 @@ constexpr int kItems = kCap / kThreads;                     // 16 keys per threa
 constexpr int kBins8 = 256;                                 // 8-bit digits: one bin per thread
 constexpr int kCluMax = 8;
 static_assert(kCap % kThreads == 0 && kBins8 == kThreads, "one bin per thread");
+// low-precision cache: per tile 128 entries x (32 B of E2M1 codes + 64 B of E4M3 codes + 2 scale bytes)
+constexpr uint32_t kQFp8Off = kTileM * 32;                 // 4 KB
+constexpr uint32_t kQScaleOff = kQFp8Off + kTileM * 64;    // 12 KB
+constexpr uint32_t kQStageBytes = kQScaleOff + kTileM * 2; // 12,544 B
+constexpr uint32_t kQOpSlots = 2;                          // bf16 operand slots (32 KB each)
+static_assert(kQOpSlots * kTileBytes + kStages * kQStageBytes <= kStages * kTileBytes, "ring layout");
 
 // Selection tables: row r of a pass's table holds CTA r's histogram of that pass (remote stores).
 // The first pass's table is written while this CTA may still be streaming: its own region. The
@@ -93,9 +107,10 @@ struct IndexSelParams {
   // the entry that t closes is pooled here (close.job[0].src non-null): KV entry by CTA 0, index
   // entry by the CTA that scores the last tile
   CompressParams close;
-  // [B, n_cap, 512] compressed KV rows, or null: each winner's row is requested into L2 as soon as it
-  // is known, so that the attention's gather of the selected rows finds them there
-  const __nv_bfloat16* ckv_prefetch;
+  // the compressed KV cache (bf16 [B, n_cap, 512] or the low-precision planes), or null: each winner's
+  // row is requested into L2 as soon as it is known, so that the attention's gather finds it there
+  const void* ckv_prefetch;
+  const uint8_t* cidx_q;        // the low-precision index cache (kLowp)
   // timeout test hook: skip the first cache-tile load and wait at most wait_ns (else 1 s)
   int test_stall;
   uint64_t wait_ns;
@@ -132,6 +147,7 @@ __device__ __forceinline__ void block_scan2(uint32_t a, uint32_t b, uint32_t* sc
   ea = wa + ia - a; eb = wb + ib - b; ta = sa; tb = sb;
 }
 
+template <bool kLowp>
 __global__ void __launch_bounds__(kThreads, 1)
     index_select_kernel(const __grid_constant__ CUtensorMap cmap, const IndexSelParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -148,7 +164,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tempty = bars + 2 * kStages + 2;                // [2]
   uint64_t* qready = bars + 2 * kStages + 4;
   uint64_t* closed = bars + 2 * kStages + 5;                // the index entry is in global memory
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 6);
+  uint64_t* opfull = bars + 2 * kStages + 6;                // [2] kLowp: bf16 operand slot written
+  uint64_t* opempty = bars + 2 * kStages + 8;               // [2] kLowp: operand slot read by the MMA
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 10);
+  uint8_t* qstage = stage_base + kQOpSlots * kTileBytes;    // kLowp: kStages x kQStageBytes
   float* w_s = reinterpret_cast<float*>(tmem_slot + 4);    // [64]
   float* red = w_s + 64;                                    // [4]
 
@@ -186,8 +205,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (et < 64) wv = p.w[(int64_t)b * 64 + et];
   }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
+    // kLowp: a staging slot is released by the 128 expanding threads, not by the MMA
+    for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kLowp ? 128 : 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&tfull[i], 1); mbar_init(&tempty[i], 128); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&opfull[i], 128); mbar_init(&opempty[i], 1); }
     mbar_init(qready, 128);
     mbar_init(closed, 64);
     fence_mbar_init();
@@ -202,19 +223,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0 && ntiles > 0) {
-      prefetch_tensormap(&cmap);
+      if (!kLowp) prefetch_tensormap(&cmap);
       const uint64_t policy = l2_evict_first_policy();      // the cache streams through once
+      const LowpLayout lay = lowp_layout(kDI, p.n_cap, 64);
+      const uint8_t* qb = kLowp ? p.cidx_q + (int64_t)b * lay.stride : nullptr;
       int issued = 0;
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages;
         if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1, p.err, p.wait_ns)) break;
         if (close_idx && i == ntiles - 1 && !mbar_wait(closed, 0, p.err, p.wait_ns)) break;   // holds entry e
         if (p.test_stall && i == 0) continue;                // the timeout test hook
-        mbar_arrive_expect_tx(&full[st], kTileBytes);
-        const int32_t y = (int32_t)(b * p.n_cap + (tile0 + i) * kTileM);
-        uint8_t* dst = stage_base + st * kTileBytes;
-        tma_load_2d_hint(dst, &cmap, &full[st], 0, y, policy);
-        tma_load_2d_hint(dst + kBlockBytes, &cmap, &full[st], 64, y, policy);
+        if constexpr (kLowp) {
+          // the tile's entries of each plane (never past n_cap; the scale run rounded up to 8
+          // entries, which the plane's 16-byte padding holds)
+          const int64_t e0 = (tile0 + i) * kTileM;
+          const uint32_t ne = (uint32_t)min((int64_t)kTileM, p.n_cap - e0), ne8 = (ne + 7) & ~7u;
+          uint8_t* dst = qstage + st * kQStageBytes;
+          mbar_arrive_expect_tx(&full[st], ne * 32 + ne * 64 + ne8 * 2);
+          bulk_load_hint(dst, qb + e0 * 32, ne * 32, &full[st], policy);
+          bulk_load_hint(dst + kQFp8Off, qb + lay.fp8 + e0 * 64, ne * 64, &full[st], policy);
+          bulk_load_hint(dst + kQScaleOff, qb + lay.scale + e0 * 2, ne8 * 2, &full[st], policy);
+        } else {
+          mbar_arrive_expect_tx(&full[st], kTileBytes);
+          const int32_t y = (int32_t)(b * p.n_cap + (tile0 + i) * kTileM);
+          uint8_t* dst = stage_base + st * kTileBytes;
+          tma_load_2d_hint(dst, &cmap, &full[st], 0, y, policy);
+          tma_load_2d_hint(dst + kBlockBytes, &cmap, &full[st], 64, y, policy);
+        }
         issued = i + 1;
       }
       // no copy may still be landing in the ring when the selection reuses it (after a wait that
@@ -229,17 +264,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_addr = smem_u32(qop);
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages, acc = i & 1;
-        if (!mbar_wait(&full[st], (i / kStages) & 1, p.err, p.wait_ns)) break;
+        if (kLowp ? !mbar_wait(&opfull[acc], (i >> 1) & 1, p.err, p.wait_ns)
+                  : !mbar_wait(&full[st], (i / kStages) & 1, p.err, p.wait_ns))
+          break;
         if (i >= 2 && !mbar_wait(&tempty[acc], ((i >> 1) & 1) ^ 1, p.err, p.wait_ns)) break;
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(stage_base + st * kTileBytes);
+        const uint32_t a_addr = smem_u32(stage_base + (kLowp ? acc : st) * kTileBytes);
         const uint32_t d = tmem + acc * 128;
 #pragma unroll
         for (int kk = 0; kk < kDI / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
           mma_bf16(d, desc_kmajor_sw128(a_addr + off), desc_kmajor_sw128(q_addr + off), kIdesc, kk > 0);
         }
-        mma_commit(&empty[st]);
+        mma_commit(kLowp ? &opempty[acc] : &empty[st]);
         mma_commit(&tfull[acc]);
       }
     }
@@ -284,9 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t quad = warp & 3;                         // TMEM lanes 32*quad .. 32*quad+31
     const int row_in_tile = quad * 32 + lane;
     float* gout = p.scores ? p.scores + (int64_t)b * p.n_cap : nullptr;
-    for (int i = 0; i < ntiles; ++i) {
+    auto epilogue = [&](int i) -> bool {
       const int acc = i & 1;
-      if (!mbar_wait_warp(&tfull[acc], (i >> 1) & 1, p.err, p.wait_ns)) break;    // uniform over the warp
+      if (!mbar_wait_warp(&tfull[acc], (i >> 1) & 1, p.err, p.wait_ns)) return false;   // uniform over the warp
       tc_fence_after();
       const uint32_t ta = tmem + ((quad * 32) << 16) + acc * 128;
       float s = 0.f;
@@ -305,17 +342,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int li = i * kTileM + row_in_tile;
       sc[li] = s;
       if (gout && li < n_local) gout[tile0 * kTileM + li] = s;
+      return true;
+    };
+    if constexpr (kLowp) {
+      // tile i: this thread expands entry row et of the staged codes into the bf16 operand slot i % 2
+      // (dims 0..63: E2M1 x the block's scale, dims 64..127: E4M3), then reduces tile i-1
+      auto expand = [&](int i) -> bool {
+        const int st = i % kStages, slot = i & 1;
+        if (!mbar_wait_warp(&full[st], (i / kStages) & 1, p.err, p.wait_ns)) return false;
+        if (i >= 2 && !mbar_wait_warp(&opempty[slot], ((i >> 1) & 1) ^ 1, p.err, p.wait_ns)) return false;
+        const uint8_t* sp = qstage + st * kQStageBytes;
+        uint8_t* op = stage_base + slot * kTileBytes;
+        const uint4 a0 = *reinterpret_cast<const uint4*>(sp + et * 32);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(sp + et * 32 + 16);
+        const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(sp + kQScaleOff + et * 2);
+        const float s0 = e8m0_to_f32(sc2 & 255u), s1 = e8m0_to_f32(sc2 >> 8);
+        const uint32_t fw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(op + sw128_offset(et, c)) = dequant_fp4x8(fw[c], c < 4 ? s0 : s1);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 f = *reinterpret_cast<const uint4*>(sp + kQFp8Off + et * 64 + j * 16);
+          *reinterpret_cast<uint4*>(op + kBlockBytes + sw128_offset(et, 2 * j)) = dequant_fp8x8(f.x, f.y);
+          *reinterpret_cast<uint4*>(op + kBlockBytes + sw128_offset(et, 2 * j + 1)) = dequant_fp8x8(f.z, f.w);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&empty[st]);
+        mbar_arrive(&opfull[slot]);
+        return true;
+      };
+      for (int i = 0; i <= ntiles; ++i) {
+        if (i < ntiles && !expand(i)) break;
+        if (i >= 1 && !epilogue(i - 1)) break;
+      }
+    } else {
+      for (int i = 0; i < ntiles; ++i)
+        if (!epilogue(i)) break;
     }
   } else {
     // ---------------------------------------------------------------- close step (warps 6, 7)
     const int ct = tid - 192;                               // 0..63
     const int64_t e = t / p.ratio;
     if (close_kv)
-      close_entry_bf16<512, 64>(p.close.job[0], p.close.N, p.n_cap, p.ratio, p.close.eps, p.close.rope, b, e, ct,
-                                red, 2);
+      close_entry_bf16<512, 64, kLowp>(p.close.job[0], p.close.N, p.n_cap, p.ratio, p.close.eps, p.close.rope, b, e,
+                                       ct, red, 2);
     if (close_idx) {
-      close_entry_bf16<128, 64>(p.close.job[1], p.close.N, p.n_cap, p.ratio, p.close.eps, p.close.rope, b, e, ct,
-                                red + 2, 2);
+      close_entry_bf16<128, 64, kLowp>(p.close.job[1], p.close.N, p.n_cap, p.ratio, p.close.eps, p.close.rope, b, e,
+                                       ct, red + 2, 2);
       fence_proxy_async_global();                           // the TMA load of the last tile reads it
       mbar_arrive(closed);
     }
@@ -418,7 +492,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (valid && !take_all && m == prefix) win = cpos++ < need;
     if (win && slot < k) {
       out[slot++] = (int32_t)(id0 + u);
-      if (p.ckv_prefetch) prefetch_l2(p.ckv_prefetch + ((int64_t)b * p.n_cap + id0 + u) * 512, 1024);
+      if (p.ckv_prefetch) {
+        const int64_t e = id0 + u;
+        if constexpr (kLowp) {                 // the entry's three pieces: 224 + 64 + 16 bytes
+          const LowpLayout kl = lowp_layout(512, p.n_cap, 64);
+          const uint8_t* kb = static_cast<const uint8_t*>(p.ckv_prefetch) + (int64_t)b * kl.stride;
+          prefetch_l2(kb + e * 224, 224);
+          prefetch_l2(kb + kl.fp8 + e * 64, 64);
+          prefetch_l2(kb + kl.scale + e * 16, 16);
+        } else {
+          prefetch_l2(static_cast<const __nv_bfloat16*>(p.ckv_prefetch) + ((int64_t)b * p.n_cap + e) * 512, 1024);
+        }
+      }
     }
   }
   const uint32_t kk = min(k, n_valid);
@@ -443,8 +528,10 @@ int tc_index_select_cluster(int B, int64_t n_cap) {
   if (c < 1) c = 1;
   static int fits[kCluMax + 1] = {0};                       // 1 = placeable, -1 = not, 0 = unknown
   if (!fits[c]) {
-    cudaError_t e = cudaFuncSetAttribute(index_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(index_select_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(index_select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     int n = 0;
     if (e == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
@@ -458,7 +545,7 @@ int tc_index_select_cluster(int B, int64_t n_cap) {
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      e = cudaOccupancyMaxActiveClusters(&n, index_select_kernel, &cfg);
+      e = cudaOccupancyMaxActiveClusters(&n, index_select_kernel<false>, &cfg);
     }
     if (e != cudaSuccess) (void)cudaGetLastError();
     fits[c] = (e == cudaSuccess && n > 0) ? 1 : -1;
@@ -469,22 +556,26 @@ int tc_index_select_cluster(int B, int64_t n_cap) {
 cudaError_t tc_index_select(int B, int C, const int64_t* pos, const void* q_idx, const float* w, const void* cidx,
                             int64_t n_cap, int ratio, int top_k, const RopeTab& rope, float* scores, int32_t* topk,
                             int32_t* err, cudaStream_t st, bool pdl, const CompressParams* close,
-                            const void* ckv_prefetch, bool test_stall) {
+                            const void* ckv_prefetch, bool test_stall, bool lowp) {
   if (C < 1 || C > kCluMax || top_k < 1) return cudaErrorInvalidValue;
   const int64_t tiles = (n_cap + kTileM - 1) / kTileM;
   if ((tiles + C - 1) / C > kMaxTiles) return cudaErrorInvalidValue;
   if ((int64_t)B * n_cap >= (int64_t)1 << 31) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(index_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(lowp ? index_select_kernel<true> : index_select_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   CUtensorMap map;
-  e = make_tmap_2d(&map, cidx, (int64_t)B * n_cap, kDI, kTileM);
-  if (e != cudaSuccess) return e;
+  memset(&map, 0, sizeof map);                                // unused with the low-precision cache
+  if (!lowp) {
+    e = make_tmap_2d(&map, cidx, (int64_t)B * n_cap, kDI, kTileM);
+    if (e != cudaSuccess) return e;
+  }
   IndexSelParams p;
   p.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
   p.w = w; p.scores = scores; p.topk = topk; p.pos = pos; p.n_cap = n_cap; p.ratio = ratio; p.k = top_k;
   p.rope = rope; p.err = err;
-  p.ckv_prefetch = static_cast<const __nv_bfloat16*>(ckv_prefetch);
+  p.ckv_prefetch = ckv_prefetch;
+  p.cidx_q = lowp ? static_cast<const uint8_t*>(cidx) : nullptr;
   p.test_stall = test_stall ? 1 : 0;
   p.wait_ns = test_stall ? 2000000ull : kWaitTimeoutNs;
   memset(&p.close, 0, sizeof p.close);
@@ -510,7 +601,7 @@ cudaError_t tc_index_select(int B, int C, const int64_t* pos, const void* q_idx,
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, index_select_kernel, map, p);
+  return cudaLaunchKernelEx(&cfg, lowp ? index_select_kernel<true> : index_select_kernel<false>, map, p);
 }
 
 }  // namespace csa

@@ -54,7 +54,7 @@ class Workload:
     ratio: int = 4
     top_k: int = 512         # 0 = HCA
     window: int = 128
-    storage: str = "bf16"    # "f32" | "bf16"
+    storage: str = "bf16"    # "f32" | "bf16" | "fp4" (bf16 raw rows, FP4 / FP8 compressed caches)
     q_gain: float = 1.0      # > 1 sharpens the attention softmax (test variants)
     seed: int = 0
 
@@ -113,7 +113,7 @@ def _draw(rng: np.random.Generator, shape, sigma: float, storage: str) -> np.nda
     a = rng.standard_normal(shape, dtype=np.float32)
     if sigma != 1.0:
         a *= np.float32(sigma)
-    return round_bf16(a) if storage == "bf16" else a
+    return a if storage == "f32" else round_bf16(a)      # "bf16", and "fp4" (bf16 raw rows)
 
 
 def gen_shared(wl: Workload) -> dict:

@@ -51,6 +51,23 @@ def test_workspace_bytes():
     assert lib.csa_workspace_bytes(ctypes.byref(hca), 16, 1, 2048) > 0
 
 
+def test_cache_bytes_match_the_format():
+    """csa_cache_bytes: plain arrays for f32 / bf16; for fp4 the stride of the oracle's own description
+    of the three-plane layout (written independently of the library)."""
+    from oracle import cache_lowp as Q
+    for n in (1, 7, 8, 2048, 16385):
+        assert L.csa_cache_bytes(L.Config(storage="bf16"), 0, n) == n * 512 * 2
+        assert L.csa_cache_bytes(L.Config(storage="f32"), 1, n) == n * 128 * 4
+        fp4 = L.Config(storage="fp4")
+        assert L.csa_cache_bytes(fp4, 0, n) == Q.cache_layout(512, n)["stride"]
+        assert L.csa_cache_bytes(fp4, 1, n) == Q.cache_layout(128, n)["stride"]
+    assert L.csa_cache_bytes(L.Config(storage="fp4"), 2, 16) == 0
+    assert L.csa_cache_bytes(L.Config(d=256), 0, 16) == 0
+    # the low-precision caches need the bf16 copies in the workspace where no fused kernel reads them
+    assert L.csa_workspace_bytes(L.Config(storage="fp4"), 1, 2, 4096) >= \
+        L.csa_workspace_bytes(L.Config(storage="bf16"), 1, 2, 4096) + 4096 * (512 + 128) * 2
+
+
 FAKE = 1 << 20          # a 16-byte aligned address that is never dereferenced
 
 
