@@ -24,7 +24,7 @@ element formats and nothing else. Readings where it is silent (listed with the d
     plane 1: n_cap x d_rope bytes, byte j = tail dim j (E4M3 code);
     plane 2: n_cap x sb bytes, byte k < L / 32 = E8M0 scale of latent dims 32k .. 32k + 31, the
              rest zero; sb = the next power of two >= L / 32 (16 for L = 448, 2 for L = 64);
-  with L = d - d_rope. Requests follow one another at a stride of
+  with L = d - d_rope (scale byte 255 is E8M0's NaN). Requests follow one another at a stride of
   n_cap (L/2 + d_rope) + n_cap sb rounded up to 16 bytes.
 """
 from __future__ import annotations
@@ -181,8 +181,12 @@ def unpack_cache(buf, d: int, n_cap: int, n: int | None = None, d_rope: int = 64
     c4[:, 0::2] = nib & 15
     c4[:, 1::2] = nib >> 4
     c8 = buf[lay["fp8"]:lay["fp8"] + n_cap * d_rope].reshape(n_cap, d_rope)[idx]
-    E = buf[lay["scale"]:lay["scale"] + n_cap * sb].reshape(n_cap, sb)[idx, :nb].astype(np.int64) - 127
-    return dequantize(c4, E, c8)
+    sbyte = buf[lay["scale"]:lay["scale"] + n_cap * sb].reshape(n_cap, sb)[idx, :nb].astype(np.int64)
+    out = dequantize(c4, sbyte - 127, c8)
+    # E8M0 byte 255 is NaN (never written by a quantiser: E <= 127)
+    nan_blk = np.repeat(sbyte == 255, 32, axis=1)
+    out[:, :L][nan_blk] = np.nan
+    return out
 
 
 def compress_lowp(kv, gate, bias, ratio: int, n_entries: int | None = None, **kw) -> np.ndarray:

@@ -116,6 +116,11 @@ def test_pack_hand_bytes_and_round_trip():
         assert b.size == Q.cache_layout(d, 9)["stride"] and b.size % 16 == 0
         np.testing.assert_array_equal(Q.unpack_cache(b, d, 9, 7), Q.lowp_round(z))
         np.testing.assert_array_equal(Q.unpack_cache(b, d, 9, entries=[6, 2]), Q.lowp_round(z)[[6, 2]])
+    # E8M0 255 is NaN: a block whose scale byte is 255 decodes to NaN, the other blocks do not
+    b = Q.pack_cache(rng.standard_normal((2, 512)), n_cap=2)
+    b[Q.cache_layout(512, 2)["scale"] + 16 + 3] = 255
+    y = Q.unpack_cache(b, 512, 2)
+    assert np.isnan(y[1, 96:128]).all() and not np.isnan(np.delete(y[1], np.s_[96:128])).any()
 
 
 def test_compress_lowp_is_the_rounded_compressor():
