@@ -13,6 +13,7 @@ NumPy oracle on the host cores on the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -82,23 +83,34 @@ def load_peaks() -> dict:
 
 
 # ----------------------------------------------------------------------------- work accounting
+def entry_bytes(wl: synth.Workload, C: int) -> int:
+    """Bytes of one compressed entry of C dims in the workload's cache storage (the FP4 / FP8 format:
+    (C - 64) / 2 bytes of E2M1 codes, 64 of E4M3 codes and the block scales: 304 for C = 512, 98 for
+    C = 128)."""
+    if wl.storage == "fp4":
+        nb = (C - wl.d_rope) // 32
+        return (C - wl.d_rope) // 2 + wl.d_rope + (16 if nb > 2 else 2)
+    return C * (4 if wl.storage == "f32" else 2)
+
+
 def decode_work(wl: synth.Workload, B: int) -> dict:
     """Algorithmic bytes / flops of one decode step of B requests (what the method must move:
     the visible index cache, the gathered candidate rows, q / q_idx / w / sink, the output, and the
     closing group of the compressor). Score round-trips and split partials are overhead, excluded."""
-    es = 2 if wl.storage == "bf16" else 4
+    es = 4 if wl.storage == "f32" else 2              # raw rows, q, out (bf16 also with fp4 caches)
     t, m = wl.t, wl.ratio
     V = (t + 1) // m
     n_win = min(wl.window, t + 1)
     n_comp = V if wl.hca else min(wl.top_k, V)
     C = n_win + n_comp
-    idx_bytes = 0 if wl.hca else B * (V * wl.d_idx * es + wl.H_idx * wl.d_idx * es + wl.H_idx * 4)
-    kv_bytes = B * C * wl.d * es
+    idx_bytes = 0 if wl.hca else B * (V * entry_bytes(wl, wl.d_idx) + wl.H_idx * wl.d_idx * es + wl.H_idx * 4)
+    kv_bytes = B * (n_win * wl.d * es + n_comp * entry_bytes(wl, wl.d))
     q_bytes = B * wl.H * wl.d * es + wl.H * 4
     out_bytes = B * wl.H * wl.d * es
     close = (t + 1) % m == 0
     chans = wl.d + (0 if wl.hca else wl.d_idx)
-    comp_bytes = B * (2 * m * chans * 2 * es + chans * es) if close else 0
+    ent = entry_bytes(wl, wl.d) + (0 if wl.hca else entry_bytes(wl, wl.d_idx))
+    comp_bytes = B * (2 * m * chans * 2 * es + ent) if close else 0
     flops_idx = 0 if wl.hca else 2 * B * wl.H_idx * wl.d_idx * V
     flops_attn = 4 * B * wl.H * C * wl.d
     return {"bytes": idx_bytes + kv_bytes + q_bytes + out_bytes + comp_bytes, "index_bytes": idx_bytes,
@@ -220,7 +232,7 @@ def device_inputs(wl: synth.Workload, requests, device):
     are drawn, so the host never holds the whole batch."""
     import torch
     B = len(requests)
-    dt = torch.bfloat16 if wl.storage == "bf16" else torch.float32
+    dt = torch.float32 if wl.storage == "f32" else torch.bfloat16
     T = {"kv": torch.empty(B, wl.N, wl.d, dtype=dt, device=device),
          "gate": torch.empty(B, wl.N, wl.d, dtype=dt, device=device),
          "q": torch.empty(B, wl.S, wl.H, wl.d, dtype=dt, device=device)}
@@ -260,22 +272,20 @@ def make_cfg(wl):
 
 
 def make_cache(T, wl, device):
-    import torch
     import long_context_sparse_19_b300 as L
     B = T["kv"].shape[0]
-    dt = T["kv"].dtype
-    ckv = torch.empty(B, wl.n_entries, wl.d, dtype=dt, device=device)
-    cidx = None if wl.hca else torch.empty(B, wl.n_entries, wl.d_idx, dtype=dt, device=device)
+    cfg = make_cfg(wl)
+    ckv = L.cache_tensor(cfg, B, wl.n_entries, 0, device=device)
+    cidx = None if wl.hca else L.cache_tensor(cfg, B, wl.n_entries, 1, device=device)
     return L.Cache(kv=T["kv"], gate=T["gate"], gate_bias=T["bias"], ckv=ckv, idx_k=T.get("idx_k"),
-                   idx_gate=T.get("idx_gate"), idx_bias=T.get("idx_bias"), cidx=cidx)
+                   idx_gate=T.get("idx_gate"), idx_bias=T.get("idx_bias"), cidx=cidx, n_cap=wl.n_entries)
 
 
 # ----------------------------------------------------------------------------- our decode leg
 def run_decode(args, world, rank, device, peaks) -> dict:
-    import dataclasses
     import torch
     import long_context_sparse_19_b300 as L
-    wl = dataclasses.replace(DECODE_WL, B=args.B) if args.B else DECODE_WL
+    wl = headline_wl(args)
     B = wl.B
     R = args.rotations
     cfg = make_cfg(wl)
@@ -291,7 +301,7 @@ def run_decode(args, world, rank, device, peaks) -> dict:
         else:
             c = L.Cache(kv=cache.kv.clone(), gate=cache.gate.clone(), gate_bias=cache.gate_bias,
                         ckv=cache.ckv.clone(), idx_k=cache.idx_k.clone(), idx_gate=cache.idx_gate.clone(),
-                        idx_bias=cache.idx_bias, cidx=cache.cidx.clone())
+                        idx_bias=cache.idx_bias, cidx=cache.cidx.clone(), n_cap=cache.n_cap)
             q, qi, w = rot[0]["q"].clone(), rot[0]["q_idx"].clone(), rot[0]["w"].clone()
         out = torch.empty(B, wl.H, wl.d, dtype=cache.kv.dtype, device=device)
         ws = L.workspace(cfg, B, 1, wl.n_entries, device=device)
@@ -367,7 +377,8 @@ def run_decode(args, world, rank, device, peaks) -> dict:
         "stage_launches": {k: v[1] for k, v in prof.items()},
         "roofline": {"kernel": "fused indexer: scores + closing entries + top-k (csa_decode stage 1)", "bound": "hbm",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": (achieved / peaks["hbm_gbs"]) if achieved else None, "traffic": index_traffic(),
+                     "frac": (achieved / peaks["hbm_gbs"]) if achieved else None,
+                     "traffic": index_traffic() if wl.storage == "bf16" else None,
                      "algorithmic_bytes_per_launch": work["index_bytes"],
                      "avg_launch_us": idx_avg_s * 1e6, "peak_source": peaks["source"]},
         "e2e": e2e,
@@ -498,16 +509,20 @@ def run_e2e(args, wl, rot, world, device) -> dict:
 
 
 # ----------------------------------------------------------------------------- every decode workload
-EXTRA_WORKLOADS = (0, 3, 4)   # the tiny fp32 decode, HCA B=16 at N=262,144, and B=4 at N=1,048,576 (+3)
+# the headline decode (B=32, N=65,536) over FP4 E2M1 + FP8 E4M3 caches: the same raw inputs
+FP4_DECODE_WL = dataclasses.replace(synth.WORKLOADS[1], name="csa_decode_fp4_B32_N65536_H64_k512", storage="fp4")
+# the tiny fp32 decode, HCA B=16 at N=262,144, B=4 at N=1,048,576 (+3), and the FP4 / FP8 cache decode
+EXTRA_WORKLOADS = {"0": synth.WORKLOADS[0], "3": synth.WORKLOADS[3], "4": synth.WORKLOADS[4], "1fp4": FP4_DECODE_WL}
 
 
 def compress_bytes(wl: synth.Workload, B: int) -> int:
     """Algorithmic bytes of a full-cache build: every raw token's rows read once (kv, gate and, for
     CSA, idx_k, idx_gate) and every entry written once."""
-    es = 2 if wl.storage == "bf16" else 4
+    es = 4 if wl.storage == "f32" else 2
     chans = wl.d + (0 if wl.hca else wl.d_idx)
     n = wl.n_entries
-    return B * (n * wl.ratio * chans * 2 * es + n * chans * es)
+    ent = entry_bytes(wl, wl.d) + (0 if wl.hca else entry_bytes(wl, wl.d_idx))
+    return B * (n * wl.ratio * chans * 2 * es + n * ent)
 
 
 def time_graph(call, K: int, W: int) -> float:
@@ -530,13 +545,11 @@ def time_graph(call, K: int, W: int) -> float:
     return e0.elapsed_time(e1) / K
 
 
-def run_decode_workload(cid: int, args, device, peaks, wl: synth.Workload | None = None) -> dict:
-    """One decode step of workload `cid` per step (CUDA graph of csa_decode), plus the full-cache
-    compressor build of the same workload and the oracle timed on the host beside it. `wl`
-    overrides the workload's shape (a reduced case, e.g. for a profiler capture)."""
+def run_decode_workload(wl: synth.Workload, args, device, peaks) -> dict:
+    """One decode step of workload `wl` per step (CUDA graph of csa_decode), plus the full-cache
+    compressor build of the same workload and the oracle timed on the host beside it."""
     import torch
     import long_context_sparse_19_b300 as L
-    wl = wl or synth.WORKLOADS[cid]
     B = wl.B
     cfg = make_cfg(wl)
     T = device_inputs(wl, list(range(B)), device)
@@ -565,7 +578,7 @@ def run_decode_workload(cid: int, args, device, peaks, wl: synth.Workload | None
             c = cache if r == 0 else L.Cache(kv=cache.kv, gate=cache.gate, gate_bias=cache.gate_bias,
                                              ckv=cache.ckv.clone(), idx_k=cache.idx_k, idx_gate=cache.idx_gate,
                                              idx_bias=cache.idx_bias,
-                                             cidx=None if wl.hca else cache.cidx.clone())
+                                             cidx=None if wl.hca else cache.cidx.clone(), n_cap=cache.n_cap)
             pos = torch.full((B,), t_r, dtype=torch.int64, device=device)
             out = torch.empty(B, wl.H, wl.d, dtype=cache.kv.dtype, device=device)
             ws = L.workspace(cfg, B, 1, wl.n_entries, device=device)
@@ -628,8 +641,13 @@ def cpu_baseline_workload(wl, T, cache, budget_s: float) -> dict:
     kv = np.zeros((t + 1, wl.d))                  # left unbacked except the window
     lo = max(0, t - wl.window + 1)
     kv[lo:t + 1] = h64(T["kv"][0, lo:t + 1])
-    ckv = h64(cache.ckv[0, :V])
-    cidx = None if wl.hca else h64(cache.cidx[0, :V])
+    if wl.storage == "fp4":                      # decoded by the oracle's unpacker (untimed)
+        from oracle import cache_lowp as Q
+        ckv = Q.unpack_cache(cache.ckv[0].cpu().numpy(), wl.d, wl.n_entries, V)
+        cidx = None if wl.hca else Q.unpack_cache(cache.cidx[0].cpu().numpy(), wl.d_idx, wl.n_entries, V)
+    else:
+        ckv = h64(cache.ckv[0, :V])
+        cidx = None if wl.hca else h64(cache.cidx[0, :V])
     q = h64(T["q"][0, 0])
     qi = None if wl.hca else h64(T["q_idx"][0, 0])
     w = None if wl.hca else h64(T["w"][0, 0])
@@ -785,8 +803,14 @@ def run_reference(args, world, rank) -> None:
 METRIC = "CSA decode query-tokens/s (N=65,536, B=32, H=64, top-k 512, W=128, bf16)"
 
 
+def headline_wl(args=None) -> synth.Workload:
+    """The decode workload of the headline leg (B=32, N=65,536; --B and --storage change it)."""
+    wl = FP4_DECODE_WL if args is not None and getattr(args, "storage", "bf16") == "fp4" else DECODE_WL
+    return dataclasses.replace(wl, B=args.B) if args is not None and args.B else wl
+
+
 def decode_config(world, args=None) -> dict:
-    wl = DECODE_WL
+    wl = headline_wl(args)
     R = args.rotations if args else ROTATIONS
     B = args.B if args and args.B else wl.B
     return {"workload": wl.name, "B_per_gpu": B, "N": wl.N, "t": wl.t, "H": wl.H, "H_idx": wl.H_idx,
@@ -809,8 +833,9 @@ def main():
     ap.add_argument("--cpu-budget-extra", type=float, default=3.0,
                     help="seconds of oracle work beside each of the other decode workloads")
     ap.add_argument("--no-workloads", action="store_true", help="skip the other decode workloads")
-    ap.add_argument("--workload", type=int, default=None, choices=(0, 1, 3, 4),
-                    help="run only this decode workload's leg (with --wl-B / --wl-N to reduce it) and print it")
+    ap.add_argument("--workload", default=None, choices=("0", "1", "3", "4", "1fp4"),
+                    help="run only this decode workload's leg (with --wl-B / --wl-N to reduce it) and print it "
+                         "(1fp4: the headline decode over FP4 / FP8 caches)")
     ap.add_argument("--wl-B", type=int, default=0, help="requests of the --workload leg (default: the workload's)")
     ap.add_argument("--wl-N", type=int, default=0,
                     help="raw tokens per request of the --workload leg (default: the workload's; the query "
@@ -819,6 +844,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--B", type=int, default=0, help="requests per GPU (default: the workload's 32)")
     ap.add_argument("--rotations", type=int, default=ROTATIONS, help="device input copies cycled between steps")
+    ap.add_argument("--storage", choices=("bf16", "fp4"), default="bf16",
+                    help="compressed-cache storage of the headline decode leg (fp4: FP4 E2M1 + FP8 E4M3)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -836,15 +863,14 @@ def main():
     device = torch.device("cuda", torch.cuda.current_device())
     peaks = load_peaks()
     if args.workload is not None:                 # one decode workload, possibly reduced
-        import dataclasses
-        wl = synth.WORKLOADS[args.workload]
+        wl = FP4_DECODE_WL if args.workload == "1fp4" else synth.WORKLOADS[int(args.workload)]
         kw = {}
         if args.wl_B:
             kw["B"] = args.wl_B
         if args.wl_N:
             kw.update(N=args.wl_N, t=args.wl_N - 1)
         wl = dataclasses.replace(wl, **kw)
-        print(json.dumps(run_decode_workload(args.workload, args, device, peaks, wl)), flush=True)
+        print(json.dumps(run_decode_workload(wl, args, device, peaks)), flush=True)
         return
     # the host-side oracle baseline runs first (rank 0, N = 1), before the GPU is busy
     cpu = None
@@ -854,7 +880,7 @@ def main():
     pre = None if args.no_prefill else run_prefill(args, device, peaks)
     extra = None
     if rank == 0 and not args.no_workloads:
-        extra = {synth.WORKLOADS[c].name: run_decode_workload(c, args, device, peaks) for c in EXTRA_WORKLOADS}
+        extra = {w.name: run_decode_workload(w, args, device, peaks) for w in EXTRA_WORKLOADS.values()}
     if rank == 0:
         line = {"metric": METRIC, "value": dec["value"], "unit": "query-tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": dec["ms_per_step"],

@@ -213,8 +213,15 @@ extern __device__ unsigned long long g_trace[8192][64];
     const int c_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);                 \
     if (c_ < 8192 && (slot) < 64) ::csa::g_trace[c_][(slot)] = t_;                                 \
   } while (0)
+// CSA_TRACE_VAL(slot, v): the value v itself in the same table (timing build only).
+#define CSA_TRACE_VAL(slot, v)                                                                     \
+  do {                                                                                             \
+    const int c_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);                 \
+    if (c_ < 8192 && (slot) < 64) ::csa::g_trace[c_][(slot)] = (unsigned long long)(v);            \
+  } while (0)
 #else
 #define CSA_STAMP(slot) ((void)0)
+#define CSA_TRACE_VAL(slot, v) ((void)0)
 #endif
 
 // visible compressed entries of a query at t

@@ -119,6 +119,38 @@ __device__ __forceinline__ uint4 dequant_fp8x8(uint32_t c0, uint32_t c1) {
   return o;
 }
 
+// f16x2 (both halves) of 2^(byte - 127): exact for E in [-24, 15] (a subnormal below 2^-14); 0 below,
+// which the codes of a block with E < -24 (values under 2^-21) then expand to.
+__device__ __forceinline__ uint32_t e8m0_to_h2(uint32_t byte) {
+  const int E = (int)byte - 127;
+  const uint32_t h = E >= -14 ? (uint32_t)(E + 15) << 10 : E >= -24 ? 1u << (E + 24) : 0u;
+  return h | (h << 16);
+}
+
+// 8 latent dims: 4 bytes of E2M1 codes times 2^E -> 8 f16 (exact for E in [-23, 13]; the expanded
+// products are exact in f16, subnormals included).
+__device__ __forceinline__ uint4 expand_fp4x8_f16(uint32_t codes, uint32_t scale2) {
+  uint4 o;
+  uint32_t* w = &o.x;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t h;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h) : "r"(codes >> (8 * j)));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(w[j]) : "r"(h), "r"(scale2));
+  }
+  return o;
+}
+
+// 8 tail dims: 8 bytes of E4M3 codes -> 8 f16 (exact: every E4M3 value is an f16 value).
+__device__ __forceinline__ uint4 expand_fp8x8_f16(uint32_t c0, uint32_t c1) {
+  uint4 o;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o.x) : "h"((uint16_t)c0));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o.y) : "h"((uint16_t)(c0 >> 16)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o.z) : "h"((uint16_t)c1));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o.w) : "h"((uint16_t)(c1 >> 16)));
+  return o;
+}
+
 // Stores this thread's P consecutive dims c0 .. c0+P-1 (P in {1, 2, 4, 8}) of entry e into the
 // request's low-precision cache at `base`. The lanes in `mask` call it together; they hold whole
 // 32-dim blocks, in lane order (lane i of an aligned group of 32 / P lanes holds dims P i .. P i + P - 1

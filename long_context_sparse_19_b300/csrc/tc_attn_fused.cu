@@ -29,8 +29,8 @@
 // the selection kernel. The code on this path runs once per CTA, where instruction fetch
 // dominates, so it is kept to short loops.
 // With the low-precision cache (FP4 E2M1 latent + FP8 E4M3 tail, lowp.cuh; 304 instead of 1024
-// bytes per entry) the selected rows are loaded into registers piece by piece (a 16-byte E2M1 piece
-// is one 32-dim block, read with its scale byte) and expanded into the same bf16 tile (exact).
+// bytes per entry) each selected row is loaded into one thread's registers (14 E2M1 pieces of one
+// 32-dim block each, the scale record, 4 E4M3 pieces) and expanded into the same bf16 tile (exact).
 // Warps: 0 = Q TMA and tcgen05.mma issuer (one lane), 1..7 gather the window rows, 1 = TMEM owner
 // and RoPE of the query, 2..7 gather the selected rows, 4..7 then run the softmax and the O
 // epilogue (lanes 0..15: one head each, TMEM lane quadrant = warp % 4); all eight merge.
@@ -205,54 +205,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     cp_async_commit();
   };
 
-  // kLowp: rows [r0, r1) from the low-precision cache, 18 pieces a row (14 E2M1 pieces of one 32-dim
-  // block each, 4 E4M3 pieces of 16 dims); a batch of pieces is loaded before any is expanded. Empty
-  // rows read as zero codes, which expand to zeros.
+  // kLowp: rows [r0, r1) from the low-precision cache, one row per thread: its 14 E2M1 pieces (one
+  // 32-dim block each), its scale record and its 4 E4M3 pieces are all loaded before any is expanded.
+  // Empty rows read as zero codes, which expand to zeros.
   auto gather_lowp = [&](int r0, int r1, int g, int ng) {
-    constexpr int kPieces = 18, kBatch = 12;
     const LowpLayout kl = lowp_layout(kD, p.n_cap, 64);
     const uint8_t* kb = static_cast<const uint8_t*>(p.ckv) + (int64_t)b * kl.stride;
-    const int n_units = (r1 - r0) * kPieces;
 #pragma unroll 1
-    for (int u0 = g; u0 < n_units; u0 += ng * kBatch) {
-      uint4 v[kBatch];
-      uint32_t sb[kBatch];
+    for (int rr = r0 + g; rr < r1; rr += ng) {
+      const int32_t gr = rows_s[rr];
+      uint4 v4[14], v8[4], sr = make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const int u = u0 + j * ng;
-        v[j] = make_uint4(0, 0, 0, 0);
-        sb[j] = 0;
-        const int32_t gr = u < n_units ? rows_s[r0 + u / kPieces] : -1;
-        if (gr >= 0) {
-          const int64_t e = gr - (int64_t)b * p.n_cap;
-          const int pc = u % kPieces;
-          if (pc < 14) {
-            v[j] = __ldcg(reinterpret_cast<const uint4*>(kb + e * 224 + pc * 16));
-            sb[j] = kb[kl.scale + e * 16 + pc];
-          } else {
-            v[j] = __ldcg(reinterpret_cast<const uint4*>(kb + kl.fp8 + e * 64 + (pc - 14) * 16));
-          }
-        }
+      for (int j = 0; j < 14; ++j) v4[j] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v8[j] = make_uint4(0, 0, 0, 0);
+      if (gr >= 0) {
+        const int64_t e = gr - (int64_t)b * p.n_cap;
+        const uint4* p4 = reinterpret_cast<const uint4*>(kb + e * 224);
+        const uint4* p8 = reinterpret_cast<const uint4*>(kb + kl.fp8 + e * 64);
+#pragma unroll
+        for (int j = 0; j < 14; ++j) v4[j] = __ldcg(p4 + j);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v8[j] = __ldcg(p8 + j);
+        sr = __ldcg(reinterpret_cast<const uint4*>(kb + kl.scale + e * 16));
+      }
+      if (g == 0 && rr == r0) CSA_STAMP(8);
+      const uint32_t sw[4] = {sr.x, sr.y, sr.z, sr.w};
+#pragma unroll
+      for (int j = 0; j < 14; ++j) {                           // dims 32 j .. 32 j + 31
+        const float sc = e8m0_to_f32((sw[j >> 2] >> (8 * (j & 3))) & 255u);
+        uint8_t* dst = kvs + (j >> 1) * kBlkStride;
+        const int c0 = (j & 1) * 4;
+        *reinterpret_cast<uint4*>(dst + sw128_offset(rr, c0 + 0)) = dequant_fp4x8(v4[j].x, sc);
+        *reinterpret_cast<uint4*>(dst + sw128_offset(rr, c0 + 1)) = dequant_fp4x8(v4[j].y, sc);
+        *reinterpret_cast<uint4*>(dst + sw128_offset(rr, c0 + 2)) = dequant_fp4x8(v4[j].z, sc);
+        *reinterpret_cast<uint4*>(dst + sw128_offset(rr, c0 + 3)) = dequant_fp4x8(v4[j].w, sc);
       }
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const int u = u0 + j * ng;
-        if (u >= n_units) continue;
-        const int rr = r0 + u / kPieces, pc = u % kPieces;
-        if (pc < 14) {                                         // dims 32 pc .. 32 pc + 31
-          const float sc = e8m0_to_f32(sb[j]);
-          uint8_t* dst = kvs + (pc >> 1) * kBlkStride;
-          const int c0 = (pc & 1) * 4;
-          *reinterpret_cast<uint4*>(dst + sw128_offset(rr, c0 + 0)) = dequant_fp4x8(v[j].x, sc);
-          *reinterpret_cast<uint4*>(dst + sw128_offset(rr, c0 + 1)) = dequant_fp4x8(v[j].y, sc);
-          *reinterpret_cast<uint4*>(dst + sw128_offset(rr, c0 + 2)) = dequant_fp4x8(v[j].z, sc);
-          *reinterpret_cast<uint4*>(dst + sw128_offset(rr, c0 + 3)) = dequant_fp4x8(v[j].w, sc);
-        } else {                                               // dims 448 + 16 q .. + 15
-          const int q = pc - 14;
-          uint8_t* dst = kvs + 7 * kBlkStride;
-          *reinterpret_cast<uint4*>(dst + sw128_offset(rr, 2 * q)) = dequant_fp8x8(v[j].x, v[j].y);
-          *reinterpret_cast<uint4*>(dst + sw128_offset(rr, 2 * q + 1)) = dequant_fp8x8(v[j].z, v[j].w);
-        }
+      for (int q = 0; q < 4; ++q) {                            // dims 448 + 16 q .. + 15
+        uint8_t* dst = kvs + 7 * kBlkStride;
+        *reinterpret_cast<uint4*>(dst + sw128_offset(rr, 2 * q)) = dequant_fp8x8(v8[q].x, v8[q].y);
+        *reinterpret_cast<uint4*>(dst + sw128_offset(rr, 2 * q + 1)) = dequant_fp8x8(v8[q].z, v8[q].w);
       }
     }
   };
@@ -347,7 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_barrier(2, kGather);                               // the row table is complete
       if constexpr (kLowp) {
         gather_lowp(p.Wc, R, gs, kGather);
+        if (gs == 0) CSA_STAMP(9);
         cp_async_wait<0>();                                    // this thread's window pieces landed
+        if (gs == 0) CSA_STAMP(10);
         rotate_own_window_pieces();
       } else {
         gather(p.Wc, R, static_cast<const __nv_bfloat16*>(p.ckv), gs, kGather);

@@ -217,7 +217,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (!mbar_wait_warp(&tfull[acc], (i >> 1) & 1, p.err)) break;    // uniform over the warp
       tc_fence_after();
       const uint32_t ta = tmem + ((quad * 32) << 16) + acc * 128;
-      float sc = 0.f;
+      // four partial sums (heads h = j mod 4): four short dependency chains instead of one of 64
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t hv[32], lv[32];
@@ -226,8 +227,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          sc = fmaf(w_s[half * 32 + j], fmaxf(__uint_as_float(hv[j]) + __uint_as_float(lv[j]), 0.f), sc);
+          s4[j & 3] = fmaf(w_s[half * 32 + j], fmaxf(__uint_as_float(hv[j]) + __uint_as_float(lv[j]), 0.f), s4[j & 3]);
       }
+      const float sc = (s4[0] + s4[1]) + (s4[2] + s4[3]);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       const int64_t e = (tile0 + i) * kTileM + quad * 32 + lane;

@@ -7,9 +7,9 @@
 // (-s_i, i)) and listed in ascending entry index, -1 padded.
 //
 // One request is one thread-block cluster of C CTAs (one CTA per SM). CTA r of the cluster scores
-// the r-th contiguous run of the request's visible 128-entry tiles, exactly as the indexer kernel
-// does it (TMA ring of cache tiles -> tcgen05.mma M = 128 entries x N = 128 (the rotated query as
-// bf16 value and bf16 remainder) x K = 128 -> TMEM -> thread-per-entry head reduction), but keeps
+// the r-th contiguous run of the request's visible 128-entry tiles (TMA ring of cache tiles ->
+// tcgen05.mma M = 128 entries x N = 128 (the rotated query as bf16 value and bf16 remainder) x
+// K = 128 -> TMEM -> thread-per-entry head reduction), but keeps
 // its scores (at most 4096) in shared memory. When every CTA of the cluster has scored its run, the
 // cluster selects the request's winners through distributed shared memory, with no global round
 // trip and no further launch. The scores become order-preserving 32-bit keys (thread t holds 16
@@ -32,10 +32,15 @@
 // waits for it) and the new KV entry in CTA 0 (the attention reads it later).
 //
 // With the low-precision cache (FP4 E2M1 dims 0..63 with two block scales, FP8 E4M3 dims 64..127;
-// lowp.cuh) a tile is three bulk copies (4 KB + 8 KB + 256 B of the cache's planes) into a staging
-// ring, and the epilogue warps first expand tile i into the bf16 operand (exact) before they reduce
-// tile i-1: the MMA sees the same operand layout as with a bf16 cache, from 98 instead of 256 bytes
-// per entry.
+// lowp.cuh) a tile is three bulk copies (4 KB + 8 KB + 256 B of the cache's planes, 98 instead of 256
+// bytes per entry) into a staging ring, and each epilogue thread first expands its TMEM lane's entry
+// of tile i into f16 (exact: an E2M1 code times a power of two and an E4M3 code are f16 values, and
+// the hardware converts both to f16 in one instruction per pair) and stores it into TMEM, where the
+// MMA takes its A operand from, before it reduces tile i-1. Shared-memory bandwidth is what an
+// expanded operand in shared memory would cost (32 KB written and read again per tile on top of the
+// query operand the MMA reads): TMEM keeps it off that path. The query operand is then f16 as well
+// (value and remainder, both f16, of the query scaled per head by a power of two that puts its
+// largest element in [256, 512); the head weight carries the inverse scale).
 //
 // Warps: 0 = TMA producer, 1 = TMEM owner and MMA issuer, 2..5 = query operand and score epilogue
 // (TMEM lane quadrant = warp % 4; with the low-precision cache also the expansion of each tile),
@@ -58,8 +63,11 @@ constexpr int kStages = 4;
 constexpr uint32_t kTileBytes = kTileM * kDI * 2;           // 32 KB: two 16 KB swizzle blocks
 constexpr uint32_t kBlockBytes = 16384;
 constexpr int kThreads = 256;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 256;                         // two accumulators of 128 columns
+// M = 128 entries x N = 128: columns 0..63 the heads' products with the query's value, 64..127 with
+// its remainder
 constexpr uint32_t kIdesc = idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdescF16 = idesc_f16(128, 128, false, false);   // low-precision cache: f16 operands
 constexpr int kMaxTiles = 32;                               // tiles per CTA
 constexpr int kCap = kMaxTiles * kTileM;                    // 4096 entries per CTA
 constexpr int kItems = kCap / kThreads;                     // 16 keys per thread
@@ -70,8 +78,12 @@ static_assert(kCap % kThreads == 0 && kBins8 == kThreads, "one bin per thread");
 constexpr uint32_t kQFp8Off = kTileM * 32;                 // 4 KB
 constexpr uint32_t kQScaleOff = kQFp8Off + kTileM * 64;    // 12 KB
 constexpr uint32_t kQStageBytes = kQScaleOff + kTileM * 2; // 12,544 B
-constexpr uint32_t kQOpSlots = 2;                          // bf16 operand slots (32 KB each)
-static_assert(kQOpSlots * kTileBytes + kStages * kQStageBytes <= kStages * kTileBytes, "ring layout");
+// the expanded f16 tile goes to TMEM (A operand of the MMA): two slots of 64 columns after the two
+// 128-column accumulators
+constexpr uint32_t kQTmemCols = 512;
+constexpr uint32_t kQACol = 256;
+// the low-precision tiles are small (12.5 KB): more are kept in flight
+constexpr int kQStages = 10;
 
 // Selection tables: row r of a pass's table holds CTA r's histogram of that pass (remote stores).
 // The first pass's table is written while this CTA may still be streaming: its own region. The
@@ -86,13 +98,22 @@ struct SelScratch {
   uint32_t scr[64];
   uint32_t res[4];
 };
-static_assert(sizeof(SelScratch) <= kStages * kTileBytes, "the selection scratch overlays the ring");
+
 
 constexpr size_t kOffRing = kTileBytes;                                  // after the query operand
-constexpr size_t kOffScores = kOffRing + kStages * kTileBytes;
-constexpr size_t kOffSel = kOffScores + kCap * sizeof(float);
-constexpr size_t kOffBars = kOffSel + sizeof(SelShared);
-constexpr size_t kSmemBytes = 1024 /*align*/ + kOffBars + 512;
+
+// shared-memory layout of each variant: [query operand][ring][scores][selection tables][barriers ...]
+template <bool kLowp>
+struct Layout {
+  static constexpr int kSt = kLowp ? kQStages : kStages;                 // loads in flight
+  static constexpr size_t kRing = kLowp ? kQStages * kQStageBytes : kStages * kTileBytes;
+  static constexpr size_t kOffScores = kOffRing + kRing;
+  static constexpr size_t kOffSel = kOffScores + kCap * sizeof(float);
+  static constexpr size_t kOffBars = kOffSel + sizeof(SelShared);
+  static constexpr size_t kSmem = 1024 /*align*/ + kOffBars + 1024;
+  static_assert(kSmem <= 232448, "shared memory of one CTA");
+  static_assert(kRing >= sizeof(SelScratch), "the selection scratch overlays the ring");
+};
 
 struct IndexSelParams {
   const __nv_bfloat16* q_idx;   // [B, 64, 128]
@@ -150,26 +171,29 @@ __device__ __forceinline__ void block_scan2(uint32_t a, uint32_t b, uint32_t* sc
 template <bool kLowp>
 __global__ void __launch_bounds__(kThreads, 1)
     index_select_kernel(const __grid_constant__ CUtensorMap cmap, const IndexSelParams p) {
+  using Lay = Layout<kLowp>;
+  constexpr int kSt = Lay::kSt;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qop = smem;                                      // [2 blocks][128 rows][128 B]
-  uint8_t* stage_base = smem + kOffRing;                    // kStages x [2 blocks][128 rows][128 B]
-  float* sc = reinterpret_cast<float*>(smem + kOffScores);  // [kCap] scores of this CTA's entries
-  SelShared& sh = *reinterpret_cast<SelShared*>(smem + kOffSel);
+  uint8_t* stage_base = smem + kOffRing;                    // kSt x [2 blocks][128 rows][128 B]
+  float* sc = reinterpret_cast<float*>(smem + Lay::kOffScores);  // [kCap] scores of this CTA's entries
+  SelShared& sh = *reinterpret_cast<SelShared*>(smem + Lay::kOffSel);
   SelScratch& sx = *reinterpret_cast<SelScratch*>(stage_base);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
-  uint64_t* full = bars;                                    // [kStages]
-  uint64_t* empty = bars + kStages;                         // [kStages]
-  uint64_t* tfull = bars + 2 * kStages;                     // [2]
-  uint64_t* tempty = bars + 2 * kStages + 2;                // [2]
-  uint64_t* qready = bars + 2 * kStages + 4;
-  uint64_t* closed = bars + 2 * kStages + 5;                // the index entry is in global memory
-  uint64_t* opfull = bars + 2 * kStages + 6;                // [2] kLowp: bf16 operand slot written
-  uint64_t* opempty = bars + 2 * kStages + 8;               // [2] kLowp: operand slot read by the MMA
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 10);
-  uint8_t* qstage = stage_base + kQOpSlots * kTileBytes;    // kLowp: kStages x kQStageBytes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kOffBars);
+  uint64_t* full = bars;                                    // [kSt]
+  uint64_t* empty = bars + kSt;                         // [kSt]
+  uint64_t* tfull = bars + 2 * kSt;                     // [2]
+  uint64_t* tempty = bars + 2 * kSt + 2;                // [2]
+  uint64_t* qready = bars + 2 * kSt + 4;
+  uint64_t* closed = bars + 2 * kSt + 5;                // the index entry is in global memory
+  uint64_t* opfull = bars + 2 * kSt + 6;                // [2] kLowp: TMEM operand slot written
+  uint64_t* opempty = bars + 2 * kSt + 8;               // [2] kLowp: operand slot read by the MMA
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kSt + 10);
+  uint8_t* qstage = stage_base;                             // kLowp: kSt x kQStageBytes
   float* w_s = reinterpret_cast<float*>(tmem_slot + 4);    // [64]
   float* red = w_s + 64;                                    // [4]
+  float* hsc = red + 4;                                     // [64] kLowp: inverse query scale per head
 
   if (threadIdx.x == 0) CSA_STAMP(42);
   griddep_launch();
@@ -206,14 +230,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     // kLowp: a staging slot is released by the 128 expanding threads, not by the MMA
-    for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kLowp ? 128 : 1); }
+    for (int i = 0; i < kSt; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kLowp ? 128 : 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&tfull[i], 1); mbar_init(&tempty[i], 128); }
     for (int i = 0; i < 2; ++i) { mbar_init(&opfull[i], 128); mbar_init(&opempty[i], 1); }
     mbar_init(qready, 128);
     mbar_init(closed, 64);
     fence_mbar_init();
   }
-  if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
+  constexpr uint32_t kCols = kLowp ? kQTmemCols : kTmemCols;
+  if (warp == 1) { tmem_alloc(tmem_slot, kCols); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -229,8 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* qb = kLowp ? p.cidx_q + (int64_t)b * lay.stride : nullptr;
       int issued = 0;
       for (int i = 0; i < ntiles; ++i) {
-        const int st = i % kStages;
-        if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1, p.err, p.wait_ns)) break;
+        const int st = i % kSt;
+        if (i >= kSt && !mbar_wait(&empty[st], ((i / kSt) & 1) ^ 1, p.err, p.wait_ns)) break;
         if (close_idx && i == ntiles - 1 && !mbar_wait(closed, 0, p.err, p.wait_ns)) break;   // holds entry e
         if (p.test_stall && i == 0) continue;                // the timeout test hook
         if constexpr (kLowp) {
@@ -251,11 +276,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d_hint(dst + kBlockBytes, &cmap, &full[st], 64, y, policy);
         }
         issued = i + 1;
+        if (i == 16) CSA_STAMP(55);
       }
       // no copy may still be landing in the ring when the selection reuses it (after a wait that
       // ran out, loads can be left unconsumed): wait, bounded, for the last load of every stage
-      for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-        if (!(p.test_stall && i == 0)) mbar_wait(&full[i % kStages], (i / kStages) & 1, p.err, p.wait_ns);
+      for (int i = issued > kSt ? issued - kSt : 0; i < issued; ++i)
+        if (!(p.test_stall && i == 0)) mbar_wait(&full[i % kSt], (i / kSt) & 1, p.err, p.wait_ns);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
@@ -263,18 +289,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t q_addr = smem_u32(qop);
       for (int i = 0; i < ntiles; ++i) {
-        const int st = i % kStages, acc = i & 1;
+        const int st = i % kSt, acc = i & 1;
         if (kLowp ? !mbar_wait(&opfull[acc], (i >> 1) & 1, p.err, p.wait_ns)
-                  : !mbar_wait(&full[st], (i / kStages) & 1, p.err, p.wait_ns))
+                  : !mbar_wait(&full[st], (i / kSt) & 1, p.err, p.wait_ns))
           break;
         if (i >= 2 && !mbar_wait(&tempty[acc], ((i >> 1) & 1) ^ 1, p.err, p.wait_ns)) break;
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(stage_base + (kLowp ? acc : st) * kTileBytes);
         const uint32_t d = tmem + acc * 128;
+        if constexpr (kLowp) {                                // A (the expanded tile) in TMEM
+          const uint32_t a_tm = tmem + kQACol + acc * 64;
 #pragma unroll
-        for (int kk = 0; kk < kDI / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-          mma_bf16(d, desc_kmajor_sw128(a_addr + off), desc_kmajor_sw128(q_addr + off), kIdesc, kk > 0);
+          for (int kk = 0; kk < kDI / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
+            mma_f16_tmem_a(d, a_tm + kk * 8, desc_kmajor_sw128(q_addr + off), kIdescF16, kk > 0);
+          }
+        } else {
+          const uint32_t a_addr = smem_u32(stage_base + st * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kDI / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
+            mma_bf16(d, desc_kmajor_sw128(a_addr + off), desc_kmajor_sw128(q_addr + off), kIdesc, kk > 0);
+          }
         }
         mma_commit(kLowp ? &opempty[acc] : &empty[st]);
         mma_commit(&tfull[acc]);
@@ -302,17 +337,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           x[2 * k + 1] = a * sn4[k] + bb * cs4[k];
         }
       }
-      float hi[8], lo[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        hi[k] = __bfloat162float(__float2bfloat16_rn(x[k]));
-        lo[k] = x[k] - hi[k];
-      }
       const int h = qh0 + 8 * i, blk = qc >> 3, ch = qc & 7;
-      store8(reinterpret_cast<__nv_bfloat16*>(qop + blk * kBlockBytes + sw128_offset(h, ch)), hi);
-      store8(reinterpret_cast<__nv_bfloat16*>(qop + blk * kBlockBytes + sw128_offset(64 + h, ch)), lo);
+      if constexpr (kLowp) {
+        // head h's 128 dims sit in the 16 lanes that share qh0: scale them by 2^sh so that the
+        // largest lies in [256, 512), then split into f16 value and f16 remainder
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(x[k]));
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const int ef = (int)((__float_as_uint(amax) >> 23) & 255u) - 127;
+        const int sh = amax > 0.f ? max(-126, min(126, 8 - ef)) : 0;
+        const float scl = __uint_as_float((uint32_t)(sh + 127) << 23);
+        uint4 uh, ul;
+        uint32_t* ph = &uh.x;
+        uint32_t* pl = &ul.x;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float a = x[2 * k] * scl, bb = x[2 * k + 1] * scl;
+          const __half2 hv = __floats2half2_rn(a, bb);
+          const float2 hf = __half22float2(hv);
+          const __half2 lv = __floats2half2_rn(a - hf.x, bb - hf.y);
+          ph[k] = *reinterpret_cast<const uint32_t*>(&hv);
+          pl[k] = *reinterpret_cast<const uint32_t*>(&lv);
+        }
+        *reinterpret_cast<uint4*>(qop + blk * kBlockBytes + sw128_offset(h, ch)) = uh;
+        *reinterpret_cast<uint4*>(qop + blk * kBlockBytes + sw128_offset(64 + h, ch)) = ul;
+        if (qc == 0) hsc[h] = __uint_as_float((uint32_t)(127 - sh) << 23);
+      } else {
+        float hi[8], lo[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          hi[k] = __bfloat162float(__float2bfloat16_rn(x[k]));
+          lo[k] = x[k] - hi[k];
+        }
+        store8(reinterpret_cast<__nv_bfloat16*>(qop + blk * kBlockBytes + sw128_offset(h, ch)), hi);
+        store8(reinterpret_cast<__nv_bfloat16*>(qop + blk * kBlockBytes + sw128_offset(64 + h, ch)), lo);
+      }
     }
-    if (et < 64) w_s[et] = wv;
+    if constexpr (kLowp) {
+      named_barrier(1, 128);                                // every head's scale is in hsc
+      if (et < 64) w_s[et] = wv * hsc[et];
+    } else {
+      if (et < 64) w_s[et] = wv;
+    }
     if (et == 0) CSA_STAMP(43);
     fence_proxy_async_smem();
     mbar_arrive(qready);
@@ -321,22 +389,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t quad = warp & 3;                         // TMEM lanes 32*quad .. 32*quad+31
     const int row_in_tile = quad * 32 + lane;
     float* gout = p.scores ? p.scores + (int64_t)b * p.n_cap : nullptr;
+#ifdef CSA_TRACE
+    unsigned long long tw_tf = 0;
+#endif
     auto epilogue = [&](int i) -> bool {
       const int acc = i & 1;
+#ifdef CSA_TRACE
+      const unsigned long long e0_ = global_timer_ns();
+#endif
       if (!mbar_wait_warp(&tfull[acc], (i >> 1) & 1, p.err, p.wait_ns)) return false;   // uniform over the warp
+#ifdef CSA_TRACE
+      tw_tf += global_timer_ns() - e0_;
+      if (et == 0 && i == ntiles - 1) CSA_TRACE_VAL(36, tw_tf);
+#endif
       tc_fence_after();
       const uint32_t ta = tmem + ((quad * 32) << 16) + acc * 128;
-      float s = 0.f;
-#pragma unroll
+      // four partial sums (heads h = k mod 4): four short dependency chains instead of one of 64.
+      // The loop over the two halves stays rolled: this loop and the expansion run once per tile
+      // on the same SMs as the other roles' loops, and what limits them is instruction fetch
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+      const float4* w4 = reinterpret_cast<const float4*>(w_s);
+#pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         uint32_t hv[32], lv[32];
         tmem_ld32(ta + half * 32, hv);
         tmem_ld32(ta + 64 + half * 32, lv);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          s = fmaf(w_s[half * 32 + j], fmaxf(__uint_as_float(hv[j]) + __uint_as_float(lv[j]), 0.f), s);
+        for (int j = 0; j < 8; ++j) {
+          const float4 wj = w4[half * 8 + j];
+          const float wv4[4] = {wj.x, wj.y, wj.z, wj.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            s4[k] = fmaf(wv4[k], fmaxf(__uint_as_float(hv[4 * j + k]) + __uint_as_float(lv[4 * j + k]), 0.f), s4[k]);
+        }
       }
+      const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       const int li = i * kTileM + row_in_tile;
@@ -345,37 +433,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     if constexpr (kLowp) {
-      // tile i: this thread expands entry row et of the staged codes into the bf16 operand slot i % 2
-      // (dims 0..63: E2M1 x the block's scale, dims 64..127: E4M3), then reduces tile i-1
+      // tile i: this thread expands its TMEM lane's entry row of the staged codes (dims 0..63: E2M1 x
+      // the block's scale, dims 64..127: E4M3) into f16 operand slot i % 2 in TMEM (the A operand of
+      // the MMA: no shared-memory round trip), then reduces tile i-1
+#ifdef CSA_TRACE
+      unsigned long long tw_full = 0, tw_op = 0;
+#endif
       auto expand = [&](int i) -> bool {
-        const int st = i % kStages, slot = i & 1;
-        if (!mbar_wait_warp(&full[st], (i / kStages) & 1, p.err, p.wait_ns)) return false;
+        const int st = i % kSt, slot = i & 1;
+#ifdef CSA_TRACE
+        const unsigned long long w0_ = global_timer_ns();
+#endif
+        if (!mbar_wait_warp(&full[st], (i / kSt) & 1, p.err, p.wait_ns)) return false;
+#ifdef CSA_TRACE
+        const unsigned long long w1_ = global_timer_ns();
+#endif
         if (i >= 2 && !mbar_wait_warp(&opempty[slot], ((i >> 1) & 1) ^ 1, p.err, p.wait_ns)) return false;
-        const uint8_t* sp = qstage + st * kQStageBytes;
-        uint8_t* op = stage_base + slot * kTileBytes;
-        const uint4 a0 = *reinterpret_cast<const uint4*>(sp + et * 32);
-        const uint4 a1 = *reinterpret_cast<const uint4*>(sp + et * 32 + 16);
-        const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(sp + kQScaleOff + et * 2);
-        const float s0 = e8m0_to_f32(sc2 & 255u), s1 = e8m0_to_f32(sc2 >> 8);
-        const uint32_t fw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(op + sw128_offset(et, c)) = dequant_fp4x8(fw[c], c < 4 ? s0 : s1);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 f = *reinterpret_cast<const uint4*>(sp + kQFp8Off + et * 64 + j * 16);
-          *reinterpret_cast<uint4*>(op + kBlockBytes + sw128_offset(et, 2 * j)) = dequant_fp8x8(f.x, f.y);
-          *reinterpret_cast<uint4*>(op + kBlockBytes + sw128_offset(et, 2 * j + 1)) = dequant_fp8x8(f.z, f.w);
+#ifdef CSA_TRACE
+        if (et == 0) {
+          tw_full += w1_ - w0_;
+          tw_op += global_timer_ns() - w1_;
         }
-        fence_proxy_async_smem();
+#endif
+        tc_fence_after();                                   // the MMA that read this slot is done
+        const uint8_t* sp = qstage + st * kQStageBytes;
+        const int r = row_in_tile;                          // this thread's TMEM lane
+        const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(sp + kQScaleOff + r * 2);
+        const uint32_t s0 = e8m0_to_h2(sc2 & 255u), s1 = e8m0_to_h2(sc2 >> 8);
+        const uint32_t a_tm = tmem + ((quad * 32) << 16) + kQACol + slot * 64;
+        uint32_t v[32];
+        {                                                   // dims 0..63: columns 0..31 of the slot
+          const uint4 c0 = *reinterpret_cast<const uint4*>(sp + r * 32);
+          const uint4 c1 = *reinterpret_cast<const uint4*>(sp + r * 32 + 16);
+          const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 h = expand_fp4x8_f16(cw[c], c < 4 ? s0 : s1);
+            v[4 * c] = h.x; v[4 * c + 1] = h.y; v[4 * c + 2] = h.z; v[4 * c + 3] = h.w;
+          }
+          tmem_st32(a_tm, v);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {                       // dims 64..127: columns 32..63
+          const uint4 f = *reinterpret_cast<const uint4*>(sp + kQFp8Off + r * 64 + j * 16);
+          const uint4 h0 = expand_fp8x8_f16(f.x, f.y), h1 = expand_fp8x8_f16(f.z, f.w);
+          v[8 * j] = h0.x; v[8 * j + 1] = h0.y; v[8 * j + 2] = h0.z; v[8 * j + 3] = h0.w;
+          v[8 * j + 4] = h1.x; v[8 * j + 5] = h1.y; v[8 * j + 6] = h1.z; v[8 * j + 7] = h1.w;
+        }
+        tmem_st32(a_tm + 32, v);
+        tmem_st_wait();
+        tc_fence_before();
         mbar_arrive(&empty[st]);
         mbar_arrive(&opfull[slot]);
         return true;
       };
+#ifdef CSA_TRACE
+      unsigned long long t_exp = 0, t_epi = 0;
+#endif
       for (int i = 0; i <= ntiles; ++i) {
+#ifdef CSA_TRACE
+        const unsigned long long ta_ = global_timer_ns();
+#endif
         if (i < ntiles && !expand(i)) break;
+        if (et == 0 && (i == 8 || i == 16 || i == 24)) CSA_STAMP(50 + i / 8);
+#ifdef CSA_TRACE
+        const unsigned long long tb_ = global_timer_ns();
+#endif
         if (i >= 1 && !epilogue(i - 1)) break;
+#ifdef CSA_TRACE
+        t_exp += tb_ - ta_;
+        t_epi += global_timer_ns() - tb_;
+#endif
       }
+#ifdef CSA_TRACE
+      if (et == 0) {
+        CSA_TRACE_VAL(32, t_exp);
+        CSA_TRACE_VAL(33, t_epi);
+        CSA_TRACE_VAL(34, tw_full);
+        CSA_TRACE_VAL(35, tw_op);
+      }
+#endif
     } else {
       for (int i = 0; i < ntiles; ++i)
         if (!epilogue(i)) break;
@@ -399,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) CSA_STAMP(44);
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, kCols);
   }
 
   // ==================================================================== cluster selection
@@ -529,15 +666,16 @@ int tc_index_select_cluster(int B, int64_t n_cap) {
   static int fits[kCluMax + 1] = {0};                       // 1 = placeable, -1 = not, 0 = unknown
   if (!fits[c]) {
     cudaError_t e = cudaFuncSetAttribute(index_select_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+                                         (int)Layout<false>::kSmem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(index_select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+      e = cudaFuncSetAttribute(index_select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)Layout<true>::kSmem);
     int n = 0;
     if (e == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3((unsigned)c, 1);
       cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = kSmemBytes;
+      cfg.dynamicSmemBytes = Layout<true>::kSmem;              // the larger of the two variants
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = (unsigned)c;
@@ -545,7 +683,7 @@ int tc_index_select_cluster(int B, int64_t n_cap) {
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      e = cudaOccupancyMaxActiveClusters(&n, index_select_kernel<false>, &cfg);
+      e = cudaOccupancyMaxActiveClusters(&n, index_select_kernel<true>, &cfg);
     }
     if (e != cudaSuccess) (void)cudaGetLastError();
     fits[c] = (e == cudaSuccess && n > 0) ? 1 : -1;
@@ -561,8 +699,9 @@ cudaError_t tc_index_select(int B, int C, const int64_t* pos, const void* q_idx,
   const int64_t tiles = (n_cap + kTileM - 1) / kTileM;
   if ((tiles + C - 1) / C > kMaxTiles) return cudaErrorInvalidValue;
   if ((int64_t)B * n_cap >= (int64_t)1 << 31) return cudaErrorInvalidValue;
+  const size_t smem = lowp ? Layout<true>::kSmem : Layout<false>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(lowp ? index_select_kernel<true> : index_select_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   CUtensorMap map;
   memset(&map, 0, sizeof map);                                // unused with the low-precision cache
@@ -586,7 +725,7 @@ cudaError_t tc_index_select(int B, int C, const int64_t* pos, const void* q_idx,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)C, (unsigned)B);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
