@@ -213,6 +213,55 @@ csa_status csa_prefill(const csa_config* cfg, int32_t B, int32_t S, const csa_ca
                        void* out, int32_t* topk_out, void* ws, size_t ws_bytes,
                        cudaStream_t stream);
 
+/* ---- The exchange over entry-range shards ------------------------------------------------------
+ * One long request's compressed caches split by entry range over G shards (in a multi-device
+ * deployment, one per device; [FLASH] "少读 KV 之前，Indexer 仍要给历史打分": the selection is made on
+ * the combined scores). Shard g holds the entries [entry_base_g, entry_base_g + n_shard_g) of every
+ * request at rows 0 .. n_shard_g - 1 of its own caches. The exact global top k is the top k of the
+ * union of the shards' local top k (an entry outside its shard's local top k has k entries of its
+ * own shard above it), and the attention ("局部和压缩记忆，共用一次归一化") splits into per-shard partials
+ * merged with the sink counted once. Between the calls below, a multi-device caller all-gathers the
+ * candidates ([B, k] scores and indices per shard) and the partials ([B, H, d] and [B, H, 2] per
+ * shard); on one device the shards' outputs are simply laid out side by side. Storage bf16 or
+ * float32; one query per request. Every call is asynchronous like the others.
+ *
+ * csa_index_topk_shard: a shard's candidates: the top_k of its visible entries (visibility of the
+ *   query at pos[b], counted in global entries) under (-s, i), as local indices in ascending order
+ *   (-1 padded) in cand_idx [B, top_k] int32, and their scores in cand_score [B, top_k] float32 (-inf
+ *   for padding). Arguments otherwise as csa_index_topk with S = 1 (q_idx [B, H_idx, d_idx], w
+ *   [B, H_idx]); ws of csa_workspace_bytes(cfg, B, 1, n_shard) bytes. */
+csa_status csa_index_topk_shard(const csa_config* cfg, int32_t B, const int64_t* pos, const void* q_idx,
+                                const float* w, const void* cidx_shard, int64_t n_shard, int64_t entry_base,
+                                int32_t* cand_idx, float* cand_score, void* ws, size_t ws_bytes,
+                                cudaStream_t stream);
+
+/* csa_topk_merge: the global selection from G shards' candidates (cand_score, cand_idx: [B, G, top_k]
+ * device, as csa_index_topk_shard writes them; entry_base, n_shard: [G] HOST arrays of disjoint
+ * ranges; 1 <= G <= 8, G * top_k <= 4096): topk [B, top_k] = the top_k of all candidates under
+ * (-s, global index), global indices in ascending order, -1 padded (exactly what csa_index_topk
+ * selects on the unsharded cache with the same scores); shard_sel [B, G, top_k] (nullable) = each
+ * shard's selected entries as its local indices, ascending, -1 padded. */
+csa_status csa_topk_merge(const csa_config* cfg, int32_t B, int32_t G, const float* cand_score,
+                          const int32_t* cand_idx, const int64_t* entry_base, const int64_t* n_shard,
+                          int32_t* topk, int32_t* shard_sel, cudaStream_t stream);
+
+/* csa_sparse_attn_shard: a shard's attention partials for the query at pos[b] over its selected rows
+ * sel [B, top_k] (local indices, -1 = empty; ignored for HCA, which takes every visible entry of the
+ * shard) and, when with_window != 0, the raw window rows of kv (one shard owns the window):
+ *   part_ml [B, H, 2] float32 = (m_h, l_h): m_h the largest logit softmax_scale * rope(q_h, t) . e_c
+ *   (-inf when the shard contributes nothing), l_h = sum_c exp(l_hc - m_h);
+ *   part_o  [B, H, d] float32 = sum_c exp(l_hc - m_h) e_c (unnormalised, in the rotated frame). */
+csa_status csa_sparse_attn_shard(const csa_config* cfg, int32_t B, const int64_t* pos, const void* q,
+                                 const void* kv, int64_t N, const void* ckv_shard, int64_t n_shard,
+                                 int64_t entry_base, const int32_t* sel, int32_t with_window, float* part_o,
+                                 float* part_ml, cudaStream_t stream);
+
+/* csa_attn_merge: out [B, H, d] (storage dtype) from G shards' partials (part_o [B, G, H, d],
+ * part_ml [B, G, H, 2], as csa_sparse_attn_shard writes them): with M = max(sink_h, m_g),
+ * o = sum_g e^(m_g - M) part_o_g / (e^(sink_h - M) + sum_g e^(m_g - M) l_g), rotated back by -t. */
+csa_status csa_attn_merge(const csa_config* cfg, int32_t B, int32_t G, const int64_t* pos, const float* part_o,
+                          const float* part_ml, const float* sink, void* out, cudaStream_t stream);
+
 /* ---- For callers that cannot allocate device memory ------------------------------------------
  * The source pages have no counterpart of this call: it is a deployment convenience of the
  * library, computing exactly what csa_index_topk computes.

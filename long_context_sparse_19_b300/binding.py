@@ -27,6 +27,7 @@ EXPORTS = ("csa_status_string", "csa_last_error", "csa_get_device_status", "csa_
            "csa_cache_bytes",
            "csa_compress", "csa_index_topk", "csa_index_topk_static", "csa_sparse_attn", "csa_decode",
            "csa_prefill",
+           "csa_index_topk_shard", "csa_topk_merge", "csa_sparse_attn_shard", "csa_attn_merge",
            "csa_launch_count", "csa_profile_begin", "csa_profile_end")
 STAGES = ("compress", "index", "topk", "attn", "merge")
 
@@ -80,6 +81,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.csa_decode.restype = c_int
     L.csa_prefill.argtypes = [cp, c_int32, c_int32, POINTER(CsaCache), vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
     L.csa_prefill.restype = c_int
+    L.csa_index_topk_shard.argtypes = [cp, c_int32, vp, vp, vp, vp, c_int64, c_int64, vp, vp, vp, c_size_t, vp]
+    L.csa_index_topk_shard.restype = c_int
+    L.csa_topk_merge.argtypes = [cp, c_int32, c_int32, vp, vp, POINTER(c_int64), POINTER(c_int64), vp, vp, vp]
+    L.csa_topk_merge.restype = c_int
+    L.csa_sparse_attn_shard.argtypes = [cp, c_int32, vp, vp, vp, c_int64, vp, c_int64, c_int64, vp, c_int32, vp, vp,
+                                        vp]
+    L.csa_sparse_attn_shard.restype = c_int
+    L.csa_attn_merge.argtypes = [cp, c_int32, c_int32, vp, vp, vp, vp, vp, vp]
+    L.csa_attn_merge.restype = c_int
     L.csa_launch_count.argtypes, L.csa_launch_count.restype = [], c_int64
     L.csa_profile_begin.argtypes, L.csa_profile_begin.restype = [c_int32], c_int
     L.csa_profile_end.argtypes, L.csa_profile_end.restype = [POINTER(c_float), POINTER(c_int32), c_int32], c_int
@@ -310,6 +320,56 @@ def csa_prefill(cfg: Config, cache: Cache, q, q_idx, w, sink, out, topk_out=None
         _ptr(sink, (cfg.H,), torch.float32, "sink"), _ptr(out, (B, S, cfg.H, cfg.d), cfg.dtype, "out"),
         _ptr(topk_out, (B, S, cfg.top_k), torch.int32, "topk_out"),
         _ptr(ws, None, torch.uint8, "ws"), ws.numel(), _stream(stream)), "csa_prefill")
+
+
+# ------------------------------------------------------------------------------------ entry-range shards
+def csa_index_topk_shard(cfg: Config, pos, q_idx, w, cidx_shard, entry_base: int, cand_idx, cand_score, ws=None,
+                         stream=None) -> None:
+    """A shard's candidates (local indices and their scores) for one query per request."""
+    B = pos.shape[0]
+    n = cidx_shard.shape[1]
+    ws = workspace(cfg, B, 1, n) if ws is None else ws
+    _check(load().csa_index_topk_shard(
+        ctypes.byref(cfg.c()), B, _ptr(pos, (B,), torch.int64, "pos"),
+        _ptr(q_idx, (B, cfg.H_idx, cfg.d_idx), cfg.dtype, "q_idx"), _ptr(w, (B, cfg.H_idx), torch.float32, "w"),
+        _ptr(cidx_shard, (B, n, cfg.d_idx), cfg.dtype, "cidx_shard"), n, entry_base,
+        _ptr(cand_idx, (B, cfg.top_k), torch.int32, "cand_idx"), _ptr(cand_score, (B, cfg.top_k), torch.float32,
+                                                                       "cand_score"),
+        _ptr(ws, None, torch.uint8, "ws"), ws.numel(), _stream(stream)), "csa_index_topk_shard")
+
+
+def csa_topk_merge(cfg: Config, cand_score, cand_idx, entry_base, n_shard, topk, shard_sel=None, stream=None) -> None:
+    """The global selection from the G shards' candidates [B, G, k] (entry_base, n_shard: G ints)."""
+    B, G, k = cand_idx.shape
+    eb = (c_int64 * G)(*[int(x) for x in entry_base])
+    ns = (c_int64 * G)(*[int(x) for x in n_shard])
+    _check(load().csa_topk_merge(
+        ctypes.byref(cfg.c()), B, G, _ptr(cand_score, (B, G, k), torch.float32, "cand_score"),
+        _ptr(cand_idx, (B, G, k), torch.int32, "cand_idx"), eb, ns, _ptr(topk, (B, k), torch.int32, "topk"),
+        _ptr(shard_sel, (B, G, k), torch.int32, "shard_sel"), _stream(stream)), "csa_topk_merge")
+
+
+def csa_sparse_attn_shard(cfg: Config, pos, q, kv, ckv_shard, entry_base: int, sel, with_window: bool, part_o, part_ml,
+                          stream=None) -> None:
+    """A shard's attention partials (unnormalised o, and (max logit, sum)) for one query per request."""
+    B = pos.shape[0]
+    N, n = kv.shape[1], ckv_shard.shape[1]
+    _check(load().csa_sparse_attn_shard(
+        ctypes.byref(cfg.c()), B, _ptr(pos, (B,), torch.int64, "pos"), _ptr(q, (B, cfg.H, cfg.d), cfg.dtype, "q"),
+        _ptr(kv, (B, N, cfg.d), cfg.dtype, "kv"), N, _ptr(ckv_shard, (B, n, cfg.d), cfg.dtype, "ckv_shard"), n,
+        entry_base, _ptr(sel, (B, cfg.top_k), torch.int32, "sel") if cfg.top_k else None, int(with_window),
+        _ptr(part_o, (B, cfg.H, cfg.d), torch.float32, "part_o"), _ptr(part_ml, (B, cfg.H, 2), torch.float32, "part_ml"),
+        _stream(stream)), "csa_sparse_attn_shard")
+
+
+def csa_attn_merge(cfg: Config, pos, part_o, part_ml, sink, out, stream=None) -> None:
+    """out [B, H, d] from G shards' partials [B, G, H, d] and [B, G, H, 2]."""
+    B, G = part_o.shape[0], part_o.shape[1]
+    _check(load().csa_attn_merge(
+        ctypes.byref(cfg.c()), B, G, _ptr(pos, (B,), torch.int64, "pos"),
+        _ptr(part_o, (B, G, cfg.H, cfg.d), torch.float32, "part_o"),
+        _ptr(part_ml, (B, G, cfg.H, 2), torch.float32, "part_ml"), _ptr(sink, (cfg.H,), torch.float32, "sink"),
+        _ptr(out, (B, cfg.H, cfg.d), cfg.dtype, "out"), _stream(stream)), "csa_attn_merge")
 
 
 def csa_launch_count() -> int:

@@ -308,9 +308,11 @@ csa_status run_compress(const csa_config* c, int B, const csa_cache* k, int64_t 
 csa_status run_index_topk(const csa_config* c, int B, int S, const int64_t* pos, const void* q_idx,
                           const float* w, const void* cidx, int64_t n_cap, int32_t* topk,
                           float* scores, float* scores_out, void* tk_ws, void* tc_ws, cudaStream_t st,
-                          bool pdl, const CompressParams* close = nullptr, const void* ckv_prefetch = nullptr) {
+                          bool pdl, const CompressParams* close = nullptr, const void* ckv_prefetch = nullptr,
+                          int64_t entry_base = 0) {
   const bool bf16 = bf16_io(c);
-  const int clu = fused_select_cluster(c, B, S, n_cap);     // with lowp(c): cidx is the low-precision cache
+  // with lowp(c): cidx is the low-precision cache; a shard of the entry range takes the general path
+  const int clu = entry_base == 0 ? fused_select_cluster(c, B, S, n_cap) : 0;
   if (clu > 0) {
     const RopeTab rope = make_rope(c);
     int32_t* err = device_error_word();
@@ -325,21 +327,23 @@ csa_status run_index_topk(const csa_config* c, int B, int S, const int64_t* pos,
     const RopeTab rope = make_rope(c);
     int32_t* err = device_error_word();
     cudaError_t e = launch_stage(ST_INDEX, st, [&] {
-      return tc_index_scores(B, S, pos, q_idx, w, cidx, n_cap, c->ratio, rope, scores, tc_ws, err, st, pdl, close);
+      return tc_index_scores(B, S, pos, q_idx, w, cidx, n_cap, c->ratio, rope, scores, tc_ws, err, st, pdl, close,
+                             entry_base);
     });
     if (e != cudaSuccess) return cuda_status(e, "tcgen05 indexer launch");
   } else {
     IndexParams ip;
     memset(&ip, 0, sizeof ip);
     ip.q_idx = q_idx; ip.w = w; ip.cidx = cidx; ip.scores = scores; ip.pos = pos; ip.n_cap = n_cap;
-    ip.S = S; ip.H_idx = c->H_idx; ip.ratio = c->ratio; ip.rope = make_rope(c);
+    ip.S = S; ip.H_idx = c->H_idx; ip.ratio = c->ratio; ip.rope = make_rope(c); ip.entry_base = entry_base;
     csa_status s = cuda_status(launch_stage(ST_INDEX, st, [&] { return launch_index_simt(bf16, B, ip, st, pdl); }),
                                "indexer launch");
     if (s != CSA_OK) return s;
   }
   TopkParams tp;
+  memset(&tp, 0, sizeof tp);
   tp.scores = scores; tp.topk = topk; tp.pos = pos; tp.n_cap = n_cap; tp.S = S; tp.k = c->top_k;
-  tp.ratio = c->ratio; tp.ws = tk_ws;
+  tp.ratio = c->ratio; tp.ws = tk_ws; tp.entry_base = entry_base;
   return cuda_status(launch_stage(ST_TOPK, st, [&] { return launch_topk(B, tp, st, true); }), "top-k launch");
 }
 
@@ -657,6 +661,101 @@ csa_status csa_prefill(const csa_config* cfg, int32_t B, int32_t S, const csa_ca
   }
   return run_attn(cfg, pl, B, S, nullptr, q, cache->kv, cache->N, ck, cache->n_cap, tk, sink, out,
                   ws, stream, true);
+}
+
+// ---- the exchange over entry-range shards
+csa_status csa_index_topk_shard(const csa_config* cfg, int32_t B, const int64_t* pos, const void* q_idx, const float* w,
+                                const void* cidx_shard, int64_t n_shard, int64_t entry_base, int32_t* cand_idx,
+                                float* cand_score, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  csa_status s = check_config(cfg);
+  if (s != CSA_OK) return s;
+  if (cfg->top_k == 0) return fail(CSA_ERR_INVALID_ARG, "top_k == 0 (HCA) has no indexer");
+  if (lowp(cfg)) return fail(CSA_ERR_NOT_IMPLEMENTED, "shard calls read bf16 or float32 caches");
+  if (B < 0 || B > 65535 || n_shard < 1 || entry_base < 0)
+    return fail(CSA_ERR_SHAPE, "B = %d, n_shard = %lld, entry_base = %lld", B, (long long)n_shard, (long long)entry_base);
+  CHECK_PTR(pos); CHECK_PTR(q_idx); CHECK_PTR(w); CHECK_PTR(cidx_shard); CHECK_PTR(cand_idx); CHECK_PTR(cand_score);
+  const Plan pl = make_plan(cfg, B, 1, n_shard);
+  s = check_ws(pl, ws, ws_bytes);
+  if (s != CSA_OK) return s;
+  if (B == 0) return CSA_OK;
+  float* sc = carve<float>(ws, pl.off_scores);
+  s = run_index_topk(cfg, B, 1, pos, q_idx, w, cidx_shard, n_shard, cand_idx, sc, sc, carve<char>(ws, pl.off_tksel),
+                     carve<char>(ws, pl.off_tc), stream, false, nullptr, nullptr, entry_base);
+  if (s != CSA_OK) return s;
+  return cuda_status(launch_stage(ST_TOPK, stream, [&] {
+                       return launch_pack_candidates(B, sc, n_shard, cand_idx, cand_score, cfg->top_k, stream, true);
+                     }),
+                     "candidate pack launch");
+}
+
+csa_status csa_topk_merge(const csa_config* cfg, int32_t B, int32_t G, const float* cand_score, const int32_t* cand_idx,
+                          const int64_t* entry_base, const int64_t* n_shard, int32_t* topk, int32_t* shard_sel,
+                          cudaStream_t stream) {
+  csa_status s = check_config(cfg);
+  if (s != CSA_OK) return s;
+  if (cfg->top_k == 0) return fail(CSA_ERR_INVALID_ARG, "top_k == 0 (HCA) has no selection");
+  if (B < 0 || B > 65535 || G < 1 || G > kMaxShards) return fail(CSA_ERR_SHAPE, "B = %d, G = %d (1..%d)", B, G, kMaxShards);
+  if ((int64_t)G * cfg->top_k > kMaxMergeCandidates)
+    return fail(CSA_ERR_SHAPE, "G * top_k = %d exceeds %d candidates", G * cfg->top_k, kMaxMergeCandidates);
+  if (!entry_base || !n_shard) return fail(CSA_ERR_INVALID_ARG, "entry_base / n_shard is NULL");
+  CHECK_PTR(cand_score); CHECK_PTR(cand_idx); CHECK_PTR(topk); CHECK_OPT_PTR(shard_sel);
+  MergeParams mp;
+  memset(&mp, 0, sizeof mp);
+  for (int g = 0; g < G; ++g) {
+    if (entry_base[g] < 0 || n_shard[g] < 0 || entry_base[g] + n_shard[g] > INT32_MAX)
+      return fail(CSA_ERR_SHAPE, "shard %d: entries [%lld, %lld)", g, (long long)entry_base[g],
+                  (long long)(entry_base[g] + n_shard[g]));
+    for (int h = 0; h < g; ++h)
+      if (entry_base[g] < entry_base[h] + n_shard[h] && entry_base[h] < entry_base[g] + n_shard[g])
+        return fail(CSA_ERR_SHAPE, "shards %d and %d overlap", h, g);
+    mp.base[g] = entry_base[g];
+    mp.n_shard[g] = n_shard[g];
+  }
+  if (B == 0) return CSA_OK;
+  mp.score = cand_score; mp.idx = cand_idx; mp.G = G; mp.k = cfg->top_k; mp.topk = topk; mp.shard_sel = shard_sel;
+  return cuda_status(launch_stage(ST_TOPK, stream, [&] { return launch_topk_merge(B, mp, stream, false); }),
+                     "candidate merge launch");
+}
+
+csa_status csa_sparse_attn_shard(const csa_config* cfg, int32_t B, const int64_t* pos, const void* q, const void* kv,
+                                 int64_t N, const void* ckv_shard, int64_t n_shard, int64_t entry_base,
+                                 const int32_t* sel, int32_t with_window, float* part_o, float* part_ml,
+                                 cudaStream_t stream) {
+  csa_status s = check_config(cfg);
+  if (s != CSA_OK) return s;
+  if (lowp(cfg)) return fail(CSA_ERR_NOT_IMPLEMENTED, "shard calls read bf16 or float32 caches");
+  if (B < 0 || B > 65535 || N < 1 || n_shard < 1 || entry_base < 0)
+    return fail(CSA_ERR_SHAPE, "B = %d, N = %lld, n_shard = %lld", B, (long long)N, (long long)n_shard);
+  CHECK_PTR(pos); CHECK_PTR(q); CHECK_PTR(kv); CHECK_PTR(ckv_shard); CHECK_PTR(part_o); CHECK_PTR(part_ml);
+  if (cfg->top_k > 0) CHECK_PTR(sel);
+  if (B == 0) return CSA_OK;
+  AttnParams ap;
+  memset(&ap, 0, sizeof ap);
+  ap.q = q; ap.kv = kv; ap.ckv = ckv_shard; ap.topk = cfg->top_k > 0 ? sel : nullptr; ap.pos = pos;
+  ap.part_o = part_o; ap.part_ml = part_ml; ap.N = N; ap.n_cap = n_shard; ap.entry_base = entry_base; ap.S = 1;
+  ap.H = cfg->H; ap.k = cfg->top_k; ap.ratio = cfg->ratio; ap.window = cfg->window; ap.n_split = 1;
+  ap.split_len = cfg->window + (cfg->top_k > 0 ? cfg->top_k : (int)n_shard);
+  ap.no_window = with_window ? 0 : 1; ap.partial = 1;
+  ap.scale = softmax_scale(cfg); ap.rope = make_rope(cfg); ap.err = device_error_word();
+  return cuda_status(
+      launch_stage(ST_ATTN, stream, [&] { return launch_attn_simt(bf16_io(cfg), B, ap, stream, false); }),
+      "shard attention launch");
+}
+
+csa_status csa_attn_merge(const csa_config* cfg, int32_t B, int32_t G, const int64_t* pos, const float* part_o,
+                          const float* part_ml, const float* sink, void* out, cudaStream_t stream) {
+  csa_status s = check_config(cfg);
+  if (s != CSA_OK) return s;
+  if (B < 0 || B > 65535 || G < 1 || G > 65535) return fail(CSA_ERR_SHAPE, "B = %d, G = %d", B, G);
+  CHECK_PTR(pos); CHECK_PTR(part_o); CHECK_PTR(part_ml); CHECK_PTR(sink); CHECK_PTR(out);
+  if (B == 0) return CSA_OK;
+  AttnParams ap;
+  memset(&ap, 0, sizeof ap);
+  ap.part_o = const_cast<float*>(part_o); ap.part_ml = const_cast<float*>(part_ml); ap.pos = pos; ap.sink = sink;
+  ap.out = out; ap.S = 1; ap.H = cfg->H; ap.n_split = G; ap.rope = make_rope(cfg); ap.err = device_error_word();
+  return cuda_status(
+      launch_stage(ST_MERGE, stream, [&] { return launch_attn_merge(bf16_io(cfg), B, ap, stream, false); }),
+      "partial merge launch");
 }
 
 int64_t csa_launch_count(void) { return g_launches.load(); }

@@ -71,9 +71,9 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnParams p)
     if (tid == 0) set_error(p.err, DEVERR_BAD_POS);
     return;
   }
-  const int64_t V = min(visible_entries(t, p.ratio), p.n_cap);
+  const int64_t V = visible_local(t, p.ratio, p.entry_base, p.n_cap);
   const int64_t lo = t - p.window + 1 > 0 ? t - p.window + 1 : 0;
-  const int64_t n_win = t - lo + 1;
+  const int64_t n_win = p.no_window ? 0 : t - lo + 1;
   const int64_t n_comp = p.topk ? p.k : V;
   const int64_t C = n_win + n_comp;
   const int64_t c_begin = (int64_t)split * p.split_len;
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnParams p)
   }
 
   if (h < p.H) {
-    if (p.n_split > 1) {
+    if (p.n_split > 1 || p.partial) {
       const int64_t pi = (row * p.n_split + split) * p.H + h;
 #pragma unroll
       for (int u = 0; u < kDPL; ++u) p.part_o[pi * kD + lane + 32 * u] = o_[u];

@@ -227,4 +227,12 @@ extern __device__ unsigned long long g_trace[8192][64];
 // visible compressed entries of a query at t
 __device__ __forceinline__ int64_t visible_entries(int64_t t, int ratio) { return (t + 1) / ratio; }
 
+// visible entries of a cache that holds the entry run [base, base + n) of a request at rows 0 .. n-1
+// (a shard of the entry range; base = 0 for a whole cache)
+__device__ __forceinline__ int64_t visible_local(int64_t t, int ratio, int64_t base, int64_t n) {
+  if (t < 0) return 0;
+  const int64_t v = visible_entries(t, ratio) - base;
+  return v < 0 ? 0 : (v < n ? v : n);
+}
+
 }  // namespace csa

@@ -23,7 +23,7 @@ __global__ void __launch_bounds__(kTile) index_simt_kernel(const IndexParams p) 
   griddep_wait();
   const int b = blockIdx.z, s = blockIdx.y;
   const int64_t t = p.pos ? p.pos[(int64_t)b * p.S + s] : s;
-  const int64_t V = min(visible_entries(t, p.ratio), p.n_cap);
+  const int64_t V = visible_local(t, p.ratio, p.entry_base, p.n_cap);
   const int64_t i0 = (int64_t)blockIdx.x * kTile;
   if (i0 >= V) return;
 

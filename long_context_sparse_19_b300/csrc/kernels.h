@@ -48,6 +48,7 @@ struct IndexParams {
   float* scores;         // [B, S, n_cap]
   const int64_t* pos;    // [B, S]; null: t = s
   int64_t n_cap;
+  int64_t entry_base;    // cidx holds the entries [entry_base, entry_base + n_cap) (0: all)
   int S, H_idx, ratio;
   RopeTab rope;
 };
@@ -60,6 +61,8 @@ struct TopkParams {
   int32_t* topk;         // [B, S, k]
   const int64_t* pos;    // [B, S]; null: t = s
   int64_t n_cap;
+  int64_t entry_base;    // the scores are those of entries [entry_base, entry_base + n_cap); the
+                         // selected indices are local (0 .. n_cap - 1)
   int S, k, ratio;
   void* ws;              // candidate buffers of the multi-level selection (topk_workspace_bytes)
 };
@@ -79,13 +82,35 @@ struct AttnParams {
   float* part_o;         // [B, S, n_split, H, d]   (n_split > 1)
   float* part_ml;        // [B, S, n_split, H, 2]
   int64_t N, n_cap;
+  int64_t entry_base;    // ckv holds the entries [entry_base, entry_base + n_cap); topk is local
   int S, H, k, ratio, window, n_split, split_len;
+  int no_window;         // CUDA-core kernel: leave the raw window out of the candidates
+  int partial;           // CUDA-core kernel: write the (max, sum, unnormalised o) partials even unsplit
   float scale;
   RopeTab rope;
   int32_t* err;
 };
 
 cudaError_t launch_attn_simt(bool bf16, int B, const AttnParams& p, cudaStream_t st, bool pdl);
+
+// ------------------------------------------------------------------ exchange over entry-range shards
+constexpr int kMaxShards = 8;
+constexpr int kMaxMergeCandidates = 4096;    // G * k per request
+
+struct MergeParams {
+  const float* score;                        // [B, G, k] candidate scores (-inf / NaN: empty)
+  const int32_t* idx;                        // [B, G, k] candidate entries, local to their shard (-1 empty)
+  int64_t base[kMaxShards];                  // first entry of each shard
+  int64_t n_shard[kMaxShards];               // entries of each shard
+  int G, k;
+  int32_t* topk;                             // [B, k] the global selection, ascending, -1 padded
+  int32_t* shard_sel;                        // [B, G, k] nullable: each shard's selected entries (local)
+};
+
+size_t topk_merge_smem(int G, int k);
+cudaError_t launch_pack_candidates(int B, const float* scores, int64_t n_shard, const int32_t* idx, float* cand_score,
+                                   int k, cudaStream_t st, bool pdl);
+cudaError_t launch_topk_merge(int B, const MergeParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_attn_merge(bool bf16, int B, const AttnParams& p, cudaStream_t st, bool pdl);
 
 }  // namespace csa

@@ -25,7 +25,7 @@ cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, int64_t rows, uint3
 cudaError_t tc_index_scores(int B, int S, const int64_t* pos, const void* q_idx, const float* w,
                             const void* cidx, int64_t n_cap, int ratio, const RopeTab& rope,
                             float* scores, void* ws, int32_t* err, cudaStream_t st, bool pdl,
-                            const CompressParams* close = nullptr);
+                            const CompressParams* close = nullptr, int64_t entry_base = 0);
 
 // Decode indexer and selection fused (S = 1): one cluster of C CTAs per request scores its visible
 // entries and selects the top_k (ascending entry index, -1 padded) into topk [B, top_k]; scores

@@ -53,6 +53,7 @@ struct IndexTcParams {
   float* scores;                // [B, S, n_cap]
   const int64_t* pos;           // [B, S] or null (t = s)
   int64_t n_cap;
+  int64_t entry_base;           // cidx holds the entries [entry_base, entry_base + n_cap)
   int S, ratio, chunks;
   RopeTab rope;
   int32_t* err;
@@ -84,7 +85,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int b = blockIdx.z, s = blockIdx.y;
   const int64_t row = (int64_t)b * p.S + s;
   const int64_t t = p.pos ? p.pos[row] : s;
-  const int64_t V = t < 0 ? 0 : min(visible_entries(t, p.ratio), p.n_cap);
+  const int64_t V = visible_local(t, p.ratio, p.entry_base, p.n_cap);
   const int64_t T = (V + kTileM - 1) / kTileM;
   // decode close: t completes group e = t / m, which makes entry e = V - 1 visible (uniform per CTA)
   const bool fused = p.close.job[0].src != nullptr;
@@ -289,7 +290,7 @@ int tc_sm_count() {
 
 cudaError_t tc_index_scores(int B, int S, const int64_t* pos, const void* q_idx, const float* w, const void* cidx,
                             int64_t n_cap, int ratio, const RopeTab& rope, float* scores, void*, int32_t* err,
-                            cudaStream_t st, bool pdl, const CompressParams* close) {
+                            cudaStream_t st, bool pdl, const CompressParams* close, int64_t entry_base) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(index_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
@@ -302,7 +303,9 @@ cudaError_t tc_index_scores(int B, int S, const int64_t* pos, const void* q_idx,
   IndexTcParams p;
   p.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
   p.w = w; p.scores = scores; p.pos = pos; p.n_cap = n_cap; p.S = S; p.ratio = ratio; p.rope = rope; p.err = err;
+  p.entry_base = entry_base;
   memset(&p.close, 0, sizeof p.close);
+  if (close && entry_base != 0) return cudaErrorInvalidValue;
   if (close) {
     if (S != 1 || close->n_jobs != 2 || close->job[0].C != 512 || close->job[1].C != kDI) return cudaErrorInvalidValue;
     p.close = *close;

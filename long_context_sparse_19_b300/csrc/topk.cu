@@ -36,6 +36,7 @@ struct SelParams {
   const int32_t* in_idx;     // level > 0: [rows, n_in] candidate entry indices (-1 = empty)
   int64_t n_in;              // items per row of the input (n_cap at level 0)
   const int64_t* pos;        // [rows] query positions (level 0 visibility); null: t = row % S
+  int64_t entry_base;        // level 0: the row holds the entries [entry_base, entry_base + n_in)
   int S, ratio, k;
   int chunk;                 // items per CTA (blockIdx.x selects the chunk)
   int n_chunks;
@@ -128,7 +129,7 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const SelParams p
   int n;
   if (level0) {
     const int64_t t = p.pos ? p.pos[row] : (row % p.S);
-    const int64_t V = t < 0 ? 0 : min(visible_entries(t, p.ratio), p.n_in);
+    const int64_t V = visible_local(t, p.ratio, p.entry_base, p.n_in);
     n = (int)max((int64_t)0, min((int64_t)p.chunk, V - c0));
   } else {
     n = (int)max((int64_t)0, min((int64_t)p.chunk, p.n_in - c0));
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(kCluThreads) topk_cluster_kernel(const SelPara
   int n;
   if (level0) {
     const int64_t t = p.pos ? p.pos[row] : (row % p.S);
-    const int64_t V = t < 0 ? 0 : min(visible_entries(t, p.ratio), p.n_in);
+    const int64_t V = visible_local(t, p.ratio, p.entry_base, p.n_in);
     n = (int)max((int64_t)0, min((int64_t)kCluChunk, V - c0));
   } else {
     n = (int)max((int64_t)0, min((int64_t)kCluChunk, p.n_in - c0));
@@ -619,6 +620,7 @@ cudaError_t launch_topk(int B, const TopkParams& p, cudaStream_t st, bool pdl) {
   const int64_t rows = (int64_t)B * p.S;
   SelParams s;
   s.scores = p.scores; s.in_key = nullptr; s.in_idx = nullptr; s.n_in = p.n_cap; s.pos = p.pos;
+  s.entry_base = p.entry_base;
   s.S = p.S; s.ratio = p.ratio; s.k = p.k;
   uint8_t* ws = static_cast<uint8_t*>(p.ws);
   const size_t half = topk_workspace_bytes(rows, p.n_cap, p.k) / 2;
