@@ -265,6 +265,161 @@ __device__ void compress_close(const CompressParams& p, const CompressJob& job, 
   }
 }
 
+// A long window (2m >= 128 tokens, HCA's m = 128: 256 tokens x 1 KB of kv and of gate per request)
+// is split over a cluster of P CTAs: CTA r folds the tokens [r 2m/P, (r+1) 2m/P) into per-channel
+// online-softmax states, CTA 0 merges the P states through distributed shared memory and stores the
+// entry. (One CTA per request left the step waiting ~37 us for 16 CTAs' 512 KB each.)
+constexpr int kCloseClusterMax = 8;
+
+template <typename T, int C, bool kLowp>
+__device__ void compress_close_split(const CompressParams& p, const CompressJob& job, float* sm) {
+  constexpr int CH = C / 8;                  // channel chunks
+  constexpr int G = kCloseThreads / CH;      // token groups
+  const int b = blockIdx.y;
+  const uint32_t rank = cluster_rank(), P = gridDim.x;
+  const int64_t t = p.pos[b];
+  // the early exits are uniform over the cluster (every CTA reads the same t): no CTA waits at a
+  // cluster barrier for one that left
+  if (t < 0 || t >= p.N) { if (threadIdx.x == 0 && rank == 0) set_error(p.err, DEVERR_BAD_POS); return; }
+  if ((t + 1) % p.ratio != 0) return;
+  const int64_t e = t / p.ratio;
+  if (e >= p.n_cap) { if (threadIdx.x == 0 && rank == 0) set_error(p.err, DEVERR_BAD_POS); return; }
+  const int m = p.ratio;
+  const int chunk = threadIdx.x % CH, g = threadIdx.x / CH;
+  const int c0 = chunk * 8;
+  const T* src = reinterpret_cast<const T*>(job.src) + (int64_t)b * p.N * C;
+  const T* gate = reinterpret_cast<const T*>(job.gate) + (int64_t)b * p.N * C;
+  const int q_lo = (int)(rank * 2 * m / P), q_hi = (int)((rank + 1) * 2 * m / P);
+  Stat8 st;
+  st.clear();
+  const int64_t j0 = (e - 1) * m;                  // window position q holds token j0 + q
+  for (int pp = q_lo + g; pp < q_hi; pp += 4 * G) {
+    float v[4][8], gt[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {                  // issue up to four tokens' loads first
+      const int q = pp + u * G;
+      if (q < q_hi && j0 + q >= 0) {
+        load8(src + (j0 + q) * C + c0, v[u]);
+        load8(gate + (j0 + q) * C + c0, gt[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = pp + u * G;
+      if (q < q_hi && j0 + q >= 0) {
+        float bq[8];
+        load8(job.bias + (int64_t)q * C + c0, bq);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) st.add(k, gt[u][k] + bq[k], v[u][k]);
+      }
+    }
+  }
+  float* smx = sm;
+  float* ssum = sm + G * C;
+  float* sacc = sm + 2 * G * C;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    smx[g * C + c0 + k] = st.mx[k];
+    ssum[g * C + c0 + k] = st.sum[k];
+    sacc[g * C + c0 + k] = st.acc[k];
+  }
+  __syncthreads();
+  float* part = sm + 3 * G * C;                    // [3][C] this CTA's merged state (read remotely)
+  if (threadIdx.x < C) {
+    const int c = threadIdx.x;
+    float M = -INFINITY;
+    for (int q = 0; q < G; ++q) M = fmaxf(M, smx[q * C + c]);
+    float num = 0.f, den = 0.f;
+    for (int q = 0; q < G; ++q) {
+      const float mq = smx[q * C + c];
+      if (mq == -INFINITY) continue;
+      const float a = expf(mq - M);
+      num = fmaf(sacc[q * C + c], a, num);
+      den = fmaf(ssum[q * C + c], a, den);
+    }
+    part[c] = M;
+    part[C + c] = den;
+    part[2 * C + c] = num;
+  }
+  cluster_sync();                                  // every CTA's state is in its shared memory
+  if (rank == 0) {
+    float* xs = part + 3 * C;                      // [C] pooled values
+    float* red = xs + C;                           // [32]
+    float ss = 0.f;
+    if (threadIdx.x < C) {
+      const int c = threadIdx.x;
+      float mr[kCloseClusterMax], dr[kCloseClusterMax], nr[kCloseClusterMax];
+#pragma unroll
+      for (int r = 0; r < kCloseClusterMax; ++r) {
+        if (r < (int)P) {
+          mr[r] = dsmem_ldf(dsmem_addr(&part[c], r));
+          dr[r] = dsmem_ldf(dsmem_addr(&part[C + c], r));
+          nr[r] = dsmem_ldf(dsmem_addr(&part[2 * C + c], r));
+        }
+      }
+      float M = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kCloseClusterMax; ++r)
+        if (r < (int)P) M = fmaxf(M, mr[r]);
+      float num = 0.f, den = 0.f;
+#pragma unroll
+      for (int r = 0; r < kCloseClusterMax; ++r) {
+        if (r < (int)P && mr[r] != -INFINITY) {
+          const float a = expf(mr[r] - M);
+          num = fmaf(nr[r], a, num);
+          den = fmaf(dr[r], a, den);
+        }
+      }
+      const float x = num / den;
+      xs[c] = x;
+      ss = x * x;
+    }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x < CH) {
+      float tot = 0.f;
+      for (int w = 0; w < kCloseThreads / 32; ++w) tot += red[w];
+      const float inv = 1.0f / sqrtf(tot / (float)C + p.eps);
+      float x[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x[k] = xs[c0 + k] * inv;
+      const int r0 = C - p.rope.d_rope;
+      if (c0 >= r0) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float cs, sn;
+          rope_cs(e * m, p.rope, (c0 - r0) / 2 + q, cs, sn);
+          const float a = x[2 * q], bq = x[2 * q + 1];
+          x[2 * q] = a * cs - bq * sn;
+          x[2 * q + 1] = a * sn + bq * cs;
+        }
+      }
+      if constexpr (kLowp) {
+        const LowpLayout lay = lowp_layout(C, p.n_cap, p.rope.d_rope);
+        store_entry_lowp<8>(static_cast<uint8_t*>(job.dst) + (int64_t)b * lay.stride, lay, e, c0, x,
+                            CH >= 32 ? 0xffffffffu : (1u << CH) - 1u);
+      } else {
+        T* dst = reinterpret_cast<T*>(job.dst) + ((int64_t)b * p.n_cap + e) * C;
+        store8(dst + c0, x);
+      }
+    }
+  }
+  cluster_sync();                                  // CTA 0 has read every CTA's state
+}
+
+template <typename T, bool kLowp>
+__global__ void __launch_bounds__(kCloseThreads) compress_close_split_kernel(const CompressParams p) {
+  extern __shared__ float sm[];
+  if (threadIdx.x == 0) CSA_STAMP(40);
+  griddep_launch();
+  griddep_wait();
+  const CompressJob& job = p.job[blockIdx.z];
+  if (job.C == 512) compress_close_split<T, 512, kLowp>(p, job, sm);
+  else compress_close_split<T, 128, kLowp>(p, job, sm);
+  if (threadIdx.x == 0) CSA_STAMP(41);
+}
+
 template <typename T, bool kLowp>
 __global__ void __launch_bounds__(kCloseThreads) compress_close_kernel(const CompressParams p) {
   extern __shared__ float sm[];
@@ -279,6 +434,37 @@ __global__ void __launch_bounds__(kCloseThreads) compress_close_kernel(const Com
 
 template <typename T, bool kLowp>
 cudaError_t launch_compress_t(int B, const CompressParams& p, cudaStream_t st, bool pdl) {
+  if (p.pos && 2 * p.ratio >= 128) {
+    // long windows: a cluster of P CTAs per (request, cache), 64 tokens or more each; shared memory:
+    // the partial states, this CTA's merged state [3][512], the pooled row and reduction scratch
+    // P = 4 for m = 128: the clusters of one step fit on the GPU at once (with P = 8, of 16
+    // clusters of 8 full-SM CTAs a part waited for a second wave)
+    int P = 2 * p.ratio / 64;
+    if (P > kCloseClusterMax / 2) P = kCloseClusterMax / 2;
+    const size_t smem = (size_t)(3 * kCloseThreads * 8 + 3 * 512 + 512 + 32) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(compress_close_split_kernel<T, kLowp>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)P, (unsigned)B, (unsigned)p.n_jobs);
+    cfg.blockDim = dim3(kCloseThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)P;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    int na = 1;
+    if (pdl) {
+      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[1].val.programmaticStreamSerializationAllowed = 1;
+      na = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, compress_close_split_kernel<T, kLowp>, p);
+  }
   if (p.pos) {
     // shared memory: 3 partial states x (token groups x channels), which is kCloseThreads * 8 for
     // both caches, plus the pooled row and reduction scratch

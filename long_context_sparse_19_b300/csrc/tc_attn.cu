@@ -28,6 +28,10 @@
 //        rotated at their own positions by the gather threads, each in the pieces it copied;
 //   7..  only gather: one SM issues scattered 16-byte copies faster with more warps issuing them
 //        (the CTA holds the whole SM, so the extra warps cost no occupancy).
+// HCA takes every visible entry, so a compressed tile whose 128 rows are all visible is one
+// contiguous run of the cache: it is loaded by TMA (two 64-column boxes per chunk, straight into the
+// swizzled layout) instead of 2,048 scattered copies; a partly visible tile keeps the gather, which
+// zero-fills its empty rows.
 #include <cudaTypedefs.h>
 
 #include "tc.h"
@@ -85,7 +89,8 @@ struct LoadSeq {
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const AttnTcParams p) {
+    attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap cmap,
+                   const AttnTcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qs = smem;                                          // [8 blocks][64 heads][128 B]
@@ -103,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* rows_s = reinterpret_cast<int32_t*>(bar_q + 8);     // [kMaxTiles][128] global row (-1 = empty)
   float* th_hi = reinterpret_cast<float*>(rows_s + kMaxTiles * kTile);   // [32]
   float* th_lo = th_hi + 32;                                   // [32]
-  int* tile_id = reinterpret_cast<int*>(th_lo + 32);           // [kMaxTiles]
+  int* tile_id = reinterpret_cast<int*>(th_lo + 32);           // [kMaxTiles] (+ [kMaxTiles] TMA flags)
   float* q_cs = reinterpret_cast<float*>(tile_id + 4);         // [32] cos / sin of the query's angles
   float* q_sn = q_cs + 32;                                     // [32]
   // softmax scratch lives in the Q buffer, which is dead once S^T is complete
@@ -135,6 +140,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int id = first_tile + (int)threadIdx.x;
     if (nt == 2 && first_tile < p.win_tiles) id = first_tile + 1 - (int)threadIdx.x;
     tile_id[threadIdx.x] = threadIdx.x < nt ? id : -1;
+    // HCA: a compressed tile whose rows are all visible is one contiguous run, loaded by TMA
+    const int64_t first = ((int64_t)id - p.win_tiles) * kTile;
+    tile_id[kMaxTiles + threadIdx.x] =
+        threadIdx.x < nt && !p.topk && id >= p.win_tiles && first + kTile <= V ? 1 : 0;
   }
   if (threadIdx.x < 32) { th_hi[threadIdx.x] = p.rope.th_hi[threadIdx.x]; th_lo[threadIdx.x] = p.rope.th_lo[threadIdx.x]; }
   if (threadIdx.x == 0) {
@@ -191,12 +200,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) CSA_STAMP(1);
   const uint32_t tmem = *tmem_slot;
   auto is_win = [&](int j) { return tile_id[j] < p.win_tiles; };
+  auto is_tma = [&](int j) { return tile_id[kMaxTiles + j] != 0; };
   // ---------------------------------------------------------------- the gather (warps 1..5)
   // Load i brings chunk c (dims 128c..128c+127) of the 128 rows of tile slot j into stage c: 2048
   // pieces of 16 bytes, consecutive threads on consecutive pieces of a row. Empty slots are zeros.
   const int gt = warp >= 7 ? threadIdx.x - 64 : threadIdx.x - 32;   // gather thread: warps 1..5, then 7..
   auto gather_issue = [&](int j, int c) {
     uint8_t* stage = ring + c * kChunkBytes;
+    if (is_tma(j)) {                                           // one thread, two boxes; the rest just arrive
+      if (gt == 0) {
+        mbar_arrive_expect_tx(&full[c], kChunkBytes);
+        const int32_t y = (int32_t)((int64_t)b * p.n_cap + (int64_t)(tile_id[j] - p.win_tiles) * kTile);
+        tma_load_2d(stage, &cmap, &full[c], c * 128, y);
+        tma_load_2d(stage + kBlk, &cmap, &full[c], c * 128 + 64, y);
+      }
+      cp_async_commit();
+      return;
+    }
     const __nv_bfloat16* base = is_win(j) ? p.kv : p.ckv;
     for (int u = gt; u < 2048; u += kGatherThreads) {
       const int rr = u >> 4, piece = u & 15;
@@ -234,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     fence_proxy_async_smem();
-    mbar_arrive(&full[c]);
+    if (!(is_tma(j) && gt == 0)) mbar_arrive(&full[c]);        // the TMA issuer arrived with the bytes
   };
   // loads [i0, i1) in order, up to kStages - 1 in flight per thread
   auto gather_loads = [&](int i0, int i1, bool& ok) {
@@ -472,8 +492,10 @@ cudaError_t tc_sparse_attn(int B, const AttnParams& a, void*, cudaStream_t st, b
   const int per = attn_tiles_per_cta(rows, tiles, a.k > 0);
   if (a.n_split != (tiles + per - 1) / per || !a.part_o) return cudaErrorInvalidValue;
   if ((int64_t)B * a.N >= (int64_t)1 << 31 || (int64_t)B * a.n_cap >= (int64_t)1 << 31) return cudaErrorInvalidValue;
-  CUtensorMap qmap;
+  CUtensorMap qmap, cmap;
   cudaError_t e = make_tmap_2d(&qmap, a.q, (int64_t)B * a.S * kH, kD, kH);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_2d(&cmap, a.ckv, (int64_t)B * a.n_cap, kD, kTile);   // HCA's whole compressed tiles
   if (e != cudaSuccess) return e;
   AttnTcParams p;
   p.kv = static_cast<const __nv_bfloat16*>(a.kv);
@@ -483,7 +505,7 @@ cudaError_t tc_sparse_attn(int B, const AttnParams& a, void*, cudaStream_t st, b
   p.win_tiles = (a.window + kTile - 1) / kTile; p.tiles_per_cta = per;
   p.scale = a.scale; p.rope = a.rope; p.err = a.err;
   dim3 grid((unsigned)rows, (unsigned)a.n_split);
-  return launch_kernel(pdl, attn_tc_kernel, grid, dim3(kThreads), kSmemBytes, st, qmap, p);
+  return launch_kernel(pdl, attn_tc_kernel, grid, dim3(kThreads), kSmemBytes, st, qmap, cmap, p);
 }
 
 }  // namespace csa

@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* q_cs = il_s + kH;                                     // [32] cos / sin of the query's angles
   float* q_sn = q_cs + 32;                                     // [32]
 
+  if (threadIdx.x == 0) CSA_STAMP(0);
   griddep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.y, s = blockIdx.x;
@@ -149,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     rows_s[i] = (int32_t)g;
   }
   __syncthreads();
+  if (threadIdx.x == 0) CSA_STAMP(1);
   const uint32_t tmem = *tmem_slot;
   const int n_loads = 4 * nt;                                  // per phase
   // load q of phase S: tile q/4, chunk q%4; load q of phase O (half = q / (2 nt)): tile (q % (2 nt)) / 2,
@@ -292,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + ((wq * 32) << 16);
     // TMEM loads are warp-collective: every lane loads, empty rows are masked afterwards
     bool ok = mbar_wait_warp(bar_s, 0, p.err);
+    if (et == 0) CSA_STAMP(2);
     tc_fence_after();
     float v[64];
 #pragma unroll
@@ -345,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     fence_proxy_async_smem();
     mbar_arrive(bar_p);
+    if (et == 0) CSA_STAMP(3);
     reduce_scatter64<false>(v, lane);
     red[wi * kH + 2 * lane] = v[0];
     red[wi * kH + 2 * lane + 1] = v[1];
@@ -358,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __nv_bfloat16* orow = p.out + row * kH * kD;
     for (int half = 0; half < 2; ++half) {
       ok = mbar_wait_warp(half == 0 ? bar_o0 : bar_o1, 0, p.err) && ok;
+      if (et == 0) CSA_STAMP(4 + half);
       tc_fence_after();
       for (int cc = 0; cc < 2; ++cc) {
         const int dim = (2 * half + cc) * 128 + r;
@@ -392,6 +397,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) {
+    CSA_STAMP(6);
+#ifdef CSA_TRACE
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    CSA_TRACE_VAL(7, smid + 1);
+#endif
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
