@@ -603,8 +603,8 @@ constexpr int kCapSmall = 128 * kItems;      // 2048
 
 // A row longer than one small CTA is first cut into 2048-item chunks, one 128-thread CTA each: one
 // SM moves only tens of GB/s, so spreading the first pass over many SMs is what makes it fast. The
-// chunks' winners (k per chunk, in index order) then go through further levels (16384-item chunks
-// while more than 16384 remain) until one CTA holds a row.
+// chunks' winners (k per chunk, in index order) then go through further levels (2048-item chunks for
+// k <= 512, else 16384-item chunks) until one cluster (or CTA) holds a row.
 static int64_t first_level_chunks(int64_t n_cap) { return (n_cap + kCapSmall - 1) / kCapSmall; }
 
 size_t topk_workspace_bytes(int64_t rows, int64_t n_cap, int k) {
@@ -638,7 +638,12 @@ cudaError_t launch_topk(int B, const TopkParams& p, cudaStream_t st, bool pdl) {
       return launch_select<1024>(s, rows, st, dep);
     }
     if (!ws) return cudaErrorInvalidValue;
-    const int64_t cap = level == 0 ? kCapSmall : kCapLarge;
+    // an intermediate level cuts its input into 2048-item chunks, one 128-thread CTA each, while
+    // that shrinks it at least 4x (k <= 512: the 1M-token decode goes 262,144 -> 65,536 -> 16,384
+    // candidates, then one cluster per row; one 1024-thread CTA per 16,384 items had left 16 CTAs
+    // busy for ~39 us there); larger k takes 16,384-item chunks, which shrink it at least 8x
+    const bool small = level == 0 || 4 * (int64_t)p.k <= kCapSmall;
+    const int64_t cap = small ? kCapSmall : kCapLarge;
     const int64_t chunks = (n_in + cap - 1) / cap;
     const int64_t n_out = chunks * p.k;
     uint8_t* buf = ws + (level & 1) * half;
@@ -646,7 +651,7 @@ cudaError_t launch_topk(int B, const TopkParams& p, cudaStream_t st, bool pdl) {
     s.topk = nullptr;
     s.out_key = reinterpret_cast<uint32_t*>(buf);
     s.out_idx = reinterpret_cast<int32_t*>(buf + (size_t)rows * n_out * 4);
-    cudaError_t e = level == 0 ? launch_select<128>(s, rows, st, dep) : launch_select<1024>(s, rows, st, dep);
+    cudaError_t e = small ? launch_select<128>(s, rows, st, dep) : launch_select<1024>(s, rows, st, dep);
     if (e != cudaSuccess) return e;
     s.scores = nullptr; s.pos = nullptr;
     s.in_key = s.out_key; s.in_idx = s.out_idx; s.n_in = n_out;
