@@ -110,7 +110,7 @@ struct Layout {
   static constexpr size_t kOffScores = kOffRing + kRing;
   static constexpr size_t kOffSel = kOffScores + kCap * sizeof(float);
   static constexpr size_t kOffBars = kOffSel + sizeof(SelShared);
-  static constexpr size_t kSmem = 1024 /*align*/ + kOffBars + 1024;
+  static constexpr size_t kSmem = 1024 /*align*/ + kOffBars + 1536;   // barriers, weights, tables
   static_assert(kSmem <= 232448, "shared memory of one CTA");
   static_assert(kRing >= sizeof(SelScratch), "the selection scratch overlays the ring");
 };
@@ -194,6 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* w_s = reinterpret_cast<float*>(tmem_slot + 4);    // [64]
   float* red = w_s + 64;                                    // [4]
   float* hsc = red + 4;                                     // [64] kLowp: inverse query scale per head
+  float* q_cs = hsc + 64;                                   // [32] cos / sin of the query's RoPE angles
+  float* q_sn = q_cs + 32;                                  // [32]
 
   if (threadIdx.x == 0) CSA_STAMP(42);
   griddep_launch();
@@ -320,11 +322,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rotated query (RoPE on dims 64..127 at t), split into bf16 value (rows 0..63) and bf16
     // remainder (rows 64..127) of the N = 128 operand
     const int r0 = kDI - p.rope.d_rope;
+    // each of the d_rope / 2 angles once (thread et), shared through shared memory
+    if (et < p.rope.d_rope / 2) rope_cs(t, p.rope, et, q_cs[et], q_sn[et]);
+    named_barrier(1, 128);
     float cs4[4], sn4[4];
     const bool rot = qc * 8 >= r0;
     if (rot) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) rope_cs(t, p.rope, (qc * 8 - r0) / 2 + k, cs4[k], sn4[k]);
+      for (int k = 0; k < 4; ++k) {
+        cs4[k] = q_cs[(qc * 8 - r0) / 2 + k];
+        sn4[k] = q_sn[(qc * 8 - r0) / 2 + k];
+      }
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
