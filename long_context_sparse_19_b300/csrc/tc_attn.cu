@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap cmap,
                    const AttnTcParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* qs = smem;                                          // [8 blocks][64 heads][128 B]
   uint8_t* ring = qs + kQBytes;                                // kStages x [2 blocks][128 rows][128 B]
   uint8_t* ps = ring + kStages * kChunkBytes;                  // kMaxTiles x [128 rows][128 B]

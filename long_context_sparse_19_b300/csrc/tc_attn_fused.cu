@@ -133,7 +133,7 @@ template <bool kLowp>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fused_kernel(const __grid_constant__ CUtensorMap qmap, const FusedParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* kvs = smem;                                         // [8 blocks][160 rows][128 B]
   uint8_t* qs = smem + kKvBytes;                               // Q: [8 blocks][64 heads][128 B]
   uint8_t* ps = qs;                                            // P: [3 blocks][64 heads][128 B] (after S)

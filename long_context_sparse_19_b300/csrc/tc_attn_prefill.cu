@@ -11,7 +11,8 @@
 //            tiles kept in TMEM (5 x 64 columns);
 //   softmax: per-head max over every candidate and the sink, P^T = exp(scale s - max) in bf16 (it
 //            reuses the Q buffer, dead by then), per-head denominators;
-//   phase O: O^T[dims] = sum_j KV_j^T P^T_j in two halves of 256 dims (2 x 64 TMEM columns), each
+//   phase O: O^T[dims] = sum_j KV_j^T P^T_j in two halves of 256 dims (2 x 64 TMEM columns each:
+//            half 0 after the S^T tiles, half 1 in the S^T columns, dead once P^T is written), each
 //            half normalised and written as the final output (inverse RoPE on dims 448..511).
 // The KV data streams through a 4-stage ring of 32 KB K-chunks twice (phase S, then phase O; the
 // second pass hits L2). The rows are gathered with 16-byte cp.async by six warps, up to three
@@ -47,7 +48,9 @@ constexpr uint32_t kColO = kMaxTiles * kH;          // 320: O^T half, 2 x 64 col
 constexpr uint32_t kIdescS = idesc_bf16(128, 64, false, false);
 constexpr uint32_t kIdescO = idesc_bf16(128, 64, true, true);
 constexpr size_t kAuxBytes = 5120;
-constexpr size_t kSmemBytes = 1024 + kQPBytes + kStages * kChunkBytes + kAuxBytes;
+constexpr size_t kOutStageBytes = 32 * kTile * 2;   // 8 KB: one block of 32 heads x 128 dims (bf16)
+constexpr size_t kSmemBytes = 1024 + kQPBytes + kStages * kChunkBytes + kAuxBytes + kOutStageBytes;
+static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct PrefillParams {
@@ -67,7 +70,7 @@ struct PrefillParams {
 __global__ void __launch_bounds__(kThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* qs = smem;                                          // Q: [8 blocks][64 heads][128 B]
   uint8_t* ps = smem;                                          // P^T: [5 tiles][128 rows][128 B] (after phase S)
   uint8_t* ring = smem + kQPBytes;                             // kStages x [2 blocks][128 rows][128 B]
@@ -79,7 +82,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_s = bar_q + 2;                                 // S^T complete
   uint64_t* bar_p = bar_q + 3;                                 // P^T written (128 arrivals)
   uint64_t* bar_o0 = bar_q + 4;                                // O^T half 0 complete
-  uint64_t* bar_e0 = bar_q + 5;                                // O^T half 0 read (128 arrivals)
   uint64_t* bar_o1 = bar_q + 6;                                // O^T half 1 complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_q + 8);
   int32_t* rows_s = reinterpret_cast<int32_t*>(bar_q + 10);    // [5][128] global row (-1 = empty)
@@ -90,6 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* il_s = mx_s + kH;                                     // [64] 1 / denominator
   float* q_cs = il_s + kH;                                     // [32] cos / sin of the query's angles
   float* q_sn = q_cs + 32;                                     // [32]
+  __nv_bfloat16* ostage = reinterpret_cast<__nv_bfloat16*>(ring + kStages * kChunkBytes + kAuxBytes);  // [32][128]
 
   if (threadIdx.x == 0) CSA_STAMP(0);
   griddep_launch();
@@ -114,7 +117,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_s, 1);
     mbar_init(bar_p, 128);
     mbar_init(bar_o0, 1);
-    mbar_init(bar_e0, 128);
     mbar_init(bar_o1, 1);
     fence_mbar_init();
   }
@@ -176,13 +178,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(bar_p, 0, p.err);
           if (!ok) break;
         }
-        if (q == n_loads + 2 * nt) {                            // half 1 reuses the O^T columns
-          mma_commit(bar_o0);
-          ok = mbar_wait(bar_e0, 0, p.err);
-          if (!ok) break;
-        }
+        if (q == n_loads + 2 * nt) mma_commit(bar_o0);          // half 1 goes to the dead S^T columns
         ok = mbar_wait(&full[st], fill & 1, p.err);
         if (!ok) break;
+        if (q >= 5 && q < 13) CSA_STAMP(34 + (q - 5));
         tc_fence_after();
         const uint32_t a0 = ring_addr + st * kChunkBytes;
         if (q < n_loads) {
@@ -196,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks) {
-            mma_bf16(tmem + kColO + (c & 1) * kH, desc_mnmajor_sw128(a0 + ks * 2048, kBlk),
+            mma_bf16(tmem + (c < 2 ? kColO : 0u) + (c & 1) * kH, desc_mnmajor_sw128(a0 + ks * 2048, kBlk),
                      desc_mnmajor_sw128(p_addr + j * kPBytes + ks * 2048, kBlk), kIdescO,
                      (j > 0 || ks > 0) ? 1u : 0u);
           }
@@ -270,17 +269,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(&full[st]);
     };
+    // A landed chunk is handed to the MMA before the thread waits for a free stage: that wait is
+    // for the MMA of an older chunk, so the MMAs never wait on the issue of the next loads.
     bool ok = true;
 #pragma unroll 1
     for (int q = 0; q < total; ++q) {
       const int st = q % kStages, fill = q / kStages;
-      if (fill > 0 && ok) ok = mbar_wait(&empty[st], (fill - 1) & 1, p.err);
-      if (ok) issue(q);
-      else cp_async_commit();
       if (q >= kStages - 1) {
-        cp_async_wait<kStages - 1>();                          // load q - (kStages - 1) landed
+        cp_async_wait<kStages - 2>();                          // load q - (kStages - 1) landed
+        if (gt == 0 && q >= 8 && q < 16) CSA_STAMP(10 + 3 * (q - 8));
         complete(q - (kStages - 1));
       }
+      if (fill > 0 && ok) ok = mbar_wait(&empty[st], (fill - 1) & 1, p.err);
+      if (gt == 0 && q >= 8 && q < 16) CSA_STAMP(11 + 3 * (q - 8));
+      if (ok) issue(q);
+      else cp_async_commit();
+      if (gt == 0 && q >= 8 && q < 16) CSA_STAMP(12 + 3 * (q - 8));
     }
     cp_async_wait<0>();
 #pragma unroll 1
@@ -358,7 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       il_s[et] = 1.f / (l + expf(p.sink[et] - mx_s[et]));
     }
     named_barrier(1, 128);
-    // two halves of O^T: thread = dim 128 c + r, 64 heads
+    // two halves of O^T: thread = dim 128 c + r, 64 heads; each block of 32 heads x 128 dims passes
+    // through shared memory and leaves as 16-byte stores (256 contiguous bytes per head)
     __nv_bfloat16* orow = p.out + row * kH * kD;
     for (int half = 0; half < 2; ++half) {
       ok = mbar_wait_warp(half == 0 ? bar_o0 : bar_o1, 0, p.err) && ok;
@@ -372,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {
           float ov[32];
-          if (ok) tmem_row32(lane_base + kColO + cc * kH + hh * 32, ov);
+          if (ok) tmem_row32(lane_base + (half == 0 ? kColO : 0u) + cc * kH + hh * 32, ov);
           else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) ov[j] = 0.f;
@@ -385,13 +390,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float y = __shfl_xor_sync(0xffffffffu, x, 1);
               x = (lane & 1) ? (x * cs - y * sn) : (x * cs + y * sn);
             }
-            orow[(int64_t)h * kD + dim] = __float2bfloat16_rn(x);
+            ostage[j * kTile + r] = __float2bfloat16_rn(x);
           }
+          named_barrier(1, 128);                                 // staged: [32 heads][128 dims]
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int u = et + 128 * i, h = u >> 4, piece = u & 15;
+            *reinterpret_cast<uint4*>(orow + (int64_t)(hh * 32 + h) * kD + (2 * half + cc) * 128 + piece * 8) =
+                *reinterpret_cast<const uint4*>(ostage + h * kTile + piece * 8);
+          }
+          named_barrier(1, 128);                                 // the stage is free again
         }
-      }
-      if (half == 0) {
-        tc_fence_before();
-        mbar_arrive(bar_e0);
       }
     }
   }

@@ -65,7 +65,7 @@ struct IndexTcParams {
 __global__ void __launch_bounds__(kThreads, 2)
     index_tc_kernel(const __grid_constant__ CUtensorMap cmap, const IndexTcParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* qop = smem;                                      // [2 blocks][128 rows][128 B]
   uint8_t* stage_base = smem + kTileBytes;                  // kStages x [2 blocks][128 rows][128 B]
   uint64_t* bars = reinterpret_cast<uint64_t*>(stage_base + kStages * kTileBytes);

@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using Lay = Layout<kLowp>;
   constexpr int kSt = Lay::kSt;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* qop = smem;                                      // [2 blocks][128 rows][128 B]
   uint8_t* stage_base = smem + kOffRing;                    // kSt x [2 blocks][128 rows][128 B]
   float* sc = reinterpret_cast<float*>(smem + Lay::kOffScores);  // [kCap] scores of this CTA's entries

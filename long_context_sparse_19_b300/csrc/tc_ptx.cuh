@@ -17,6 +17,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared memory rounded up to a 1024-byte boundary (the alignment of a 128-byte swizzle
+// atom). The rounding is pointer arithmetic on the shared array itself: a round trip through an
+// integer would hide the state space from the compiler, and every access through the result would
+// become a generic load or store, which is slower than an ld / st.shared.
+__device__ __forceinline__ uint8_t* smem_align1024(uint8_t* raw) {
+  return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
