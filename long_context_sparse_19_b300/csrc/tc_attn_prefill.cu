@@ -36,6 +36,8 @@ constexpr int kTile = 128;
 constexpr int kMaxTiles = 5;
 constexpr int kThreads = 384;
 constexpr int kGatherThreads = 192;                 // warps 6..11
+constexpr int kSThreads = 320;                      // warps 2..11 during phase S
+static_assert(11 * kGatherThreads >= 2048 && kSThreads >= kGatherThreads, "a chunk in 11 rounds");
 constexpr int kStages = 4;
 constexpr uint32_t kBlk = kTile * 128;              // 16 KB: [128 rows][64 dims] swizzled
 constexpr uint32_t kChunkBytes = 2 * kBlk;          // 32 KB: 128 rows x 128 dims
@@ -75,7 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ps = smem;                                          // P^T: [5 tiles][128 rows][128 B] (after phase S)
   uint8_t* ring = smem + kQPBytes;                             // kStages x [2 blocks][128 rows][128 B]
   uint64_t* bars = reinterpret_cast<uint64_t*>(ring + kStages * kChunkBytes);
-  uint64_t* full = bars;                                       // [kStages] (kGatherThreads arrivals)
+  uint64_t* full = bars;                                       // [kStages] phase O (kGatherThreads arrivals)
   uint64_t* empty = bars + kStages;                            // [kStages] (MMA commit)
   uint64_t* bar_q = bars + 2 * kStages;                        // Q landed (tx)
   uint64_t* bar_qrot = bar_q + 1;                              // Q rotated (32 arrivals)
@@ -84,7 +86,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_o0 = bar_q + 4;                                // O^T half 0 complete
   uint64_t* bar_o1 = bar_q + 6;                                // O^T half 1 complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_q + 8);
-  int32_t* rows_s = reinterpret_cast<int32_t*>(bar_q + 10);    // [5][128] global row (-1 = empty)
+  uint64_t* full_s = bar_q + 10;                               // [kStages] phase S (kSThreads arrivals)
+  int32_t* rows_s = reinterpret_cast<int32_t*>(bar_q + 14);    // [5][128] global row (-1 = empty)
   float* th_hi = reinterpret_cast<float*>(rows_s + kMaxTiles * kTile);   // [32]
   float* th_lo = th_hi + 32;                                   // [32]
   float* red = th_lo + 32;                                     // [4][64]
@@ -111,7 +114,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x < 32) { th_hi[threadIdx.x] = p.rope.th_hi[threadIdx.x]; th_lo[threadIdx.x] = p.rope.th_lo[threadIdx.x]; }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], kGatherThreads); mbar_init(&empty[i], 1); }
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], kGatherThreads);
+      mbar_init(&full_s[i], kSThreads);
+      mbar_init(&empty[i], 1);
+    }
     mbar_init(bar_q, 1);
     mbar_init(bar_qrot, 32);
     mbar_init(bar_s, 1);
@@ -164,6 +171,88 @@ __global__ void __launch_bounds__(kThreads, 1)
     c = 2 * half + (v & 1);
   };
 
+  // ------------------------------------------------------------------ gather pipeline
+  // Load q brings chunk c (dims 128c .. 128c+127) of the 128 rows of tile j into stage q % kStages:
+  // 2048 pieces of 16 bytes, consecutive threads on consecutive pieces of a row; empty rows are
+  // zeros. A chunk of phase S is split over the 320 threads of warps 2..11 (the softmax warps have
+  // nothing else to do until S is complete), a chunk of phase O over the 192 threads of warps
+  // 6..11. After a raw window tile's chunk 3 lands (block 1 = dims 448..511), each thread rotates
+  // the pieces it copied at the row's own position.
+  auto split_of = [&](int q, int& tid, int& nth) {
+    if (q < n_loads) { tid = (int)threadIdx.x - 64; nth = kSThreads; }
+    else { tid = (int)threadIdx.x - 192; nth = kGatherThreads; }
+  };
+  auto issue = [&](int q) {
+    int j, c, tid, nth;
+    load_of(q, j, c);
+    split_of(q, tid, nth);
+    uint8_t* stage = ring + (q % kStages) * kChunkBytes;
+    const __nv_bfloat16* base = j < p.win_tiles ? p.kv : p.ckv;
+    // unrolled (11 x 192 >= 2048): the row-table reads are all issued ahead of the copies
+#pragma unroll
+    for (int i = 0; i < 11; ++i) {
+      const int u = tid + i * nth;
+      if (u < 2048) {
+        const int rr = u >> 4, piece = u & 15;
+        uint8_t* dst = stage + (piece >> 3) * kBlk + sw128_offset(rr, piece & 7);
+        const int32_t g = rows_s[j * kTile + rr];
+        if (g >= 0) cp_async16(dst, base + (int64_t)g * kD + c * 128 + piece * 8);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    cp_async_commit();
+  };
+  auto complete = [&](int q) {
+    int j, c, tid, nth;
+    load_of(q, j, c);
+    split_of(q, tid, nth);
+    const int st = q % kStages;
+    if (c == 3 && j < p.win_tiles) {
+      uint8_t* blk1 = ring + st * kChunkBytes + kBlk;
+#pragma unroll 1
+      for (int u = tid; u < 2048; u += nth) {
+        const int rr = u >> 4, piece = u & 15;
+        if (piece < 8 || rows_s[j * kTile + rr] < 0) continue;
+        uint4* q16 = reinterpret_cast<uint4*>(blk1 + sw128_offset(rr, piece - 8));
+        uint4 v = *q16;
+        uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+        const int64_t pos_r = lo + (int64_t)j * kTile + rr;
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k) {
+          const int pair = (piece - 8) * 4 + k;
+          const float2 cs = rope_cs_nl(pos_r, th_hi[pair], th_lo[pair]);
+          const float a = bf16lo(w[k]), bb = bf16hi(w[k]);
+          w[k] = pack_bf16(a * cs.x - bb * cs.y, a * cs.y + bb * cs.x);
+        }
+        *q16 = v;
+      }
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(q < n_loads ? &full_s[st] : &full[st]);
+  };
+  // Loads [0, q_end). A landed chunk is handed to the MMA before the thread waits for a free stage:
+  // that wait is for the MMA of an older chunk, so the MMAs never wait on the issue of next loads.
+  auto gather = [&](int q_end) {
+    bool ok = true;
+#pragma unroll 1
+    for (int q = 0; q < q_end; ++q) {
+      const int st = q % kStages, fill = q / kStages;
+      if (q >= kStages - 1) {
+        cp_async_wait<kStages - 2>();                          // load q - (kStages - 1) landed
+        if (threadIdx.x == 192 && q >= 8 && q < 16) CSA_STAMP(10 + 3 * (q - 8));
+        complete(q - (kStages - 1));
+      }
+      if (fill > 0 && ok) ok = mbar_wait(&empty[st], (fill - 1) & 1, p.err);
+      if (threadIdx.x == 192 && q >= 8 && q < 16) CSA_STAMP(11 + 3 * (q - 8));
+      if (ok) issue(q);
+      else cp_async_commit();
+      if (threadIdx.x == 192 && q >= 8 && q < 16) CSA_STAMP(12 + 3 * (q - 8));
+    }
+    cp_async_wait<0>();
+#pragma unroll 1
+    for (int q = q_end > kStages - 1 ? q_end - (kStages - 1) : 0; q < q_end; ++q) complete(q);
+  };
+
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
@@ -179,7 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         if (q == n_loads + 2 * nt) mma_commit(bar_o0);          // half 1 goes to the dead S^T columns
-        ok = mbar_wait(&full[st], fill & 1, p.err);
+        ok = q < n_loads ? mbar_wait(&full_s[st], fill & 1, p.err)
+                         : mbar_wait(&full[st], ((q - n_loads) / kStages) & 1, p.err);
         if (!ok) break;
         if (q >= 5 && q < 13) CSA_STAMP(34 + (q - 5));
         tc_fence_after();
@@ -220,77 +310,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
     mbar_arrive(bar_qrot);
   } else if (warp >= 6) {
-    // ---------------------------------------------------------------- gather (warps 6..11)
-    // load q brings chunk c (dims 128c .. 128c+127) of the 128 rows of tile j into stage q % kStages:
-    // 2048 pieces of 16 bytes, consecutive threads on consecutive pieces of a row; empty rows are
-    // zeros. After a raw window tile's chunk 3 lands (block 1 = dims 448..511), each thread rotates
-    // the pieces it copied at the row's own position.
-    const int gt = threadIdx.x - 192;
-    const int total = 2 * n_loads;
-    auto issue = [&](int q) {
-      int j, c;
-      load_of(q, j, c);
-      uint8_t* stage = ring + (q % kStages) * kChunkBytes;
-      const __nv_bfloat16* base = j < p.win_tiles ? p.kv : p.ckv;
-#pragma unroll 1
-      for (int u = gt; u < 2048; u += kGatherThreads) {
-        const int rr = u >> 4, piece = u & 15;
-        uint8_t* dst = stage + (piece >> 3) * kBlk + sw128_offset(rr, piece & 7);
-        const int32_t g = rows_s[j * kTile + rr];
-        if (g >= 0) cp_async16(dst, base + (int64_t)g * kD + c * 128 + piece * 8);
-        else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-      }
-      cp_async_commit();
-    };
-    auto complete = [&](int q) {
-      int j, c;
-      load_of(q, j, c);
-      const int st = q % kStages;
-      if (c == 3 && j < p.win_tiles) {
-        uint8_t* blk1 = ring + st * kChunkBytes + kBlk;
-#pragma unroll 1
-        for (int u = gt; u < 2048; u += kGatherThreads) {
-          const int rr = u >> 4, piece = u & 15;
-          if (piece < 8 || rows_s[j * kTile + rr] < 0) continue;
-          uint4* q16 = reinterpret_cast<uint4*>(blk1 + sw128_offset(rr, piece - 8));
-          uint4 v = *q16;
-          uint32_t* w = reinterpret_cast<uint32_t*>(&v);
-          const int64_t pos_r = lo + (int64_t)j * kTile + rr;
-#pragma unroll 1
-          for (int k = 0; k < 4; ++k) {
-            const int pair = (piece - 8) * 4 + k;
-            const float2 cs = rope_cs_nl(pos_r, th_hi[pair], th_lo[pair]);
-            const float a = bf16lo(w[k]), bb = bf16hi(w[k]);
-            w[k] = pack_bf16(a * cs.x - bb * cs.y, a * cs.y + bb * cs.x);
-          }
-          *q16 = v;
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&full[st]);
-    };
-    // A landed chunk is handed to the MMA before the thread waits for a free stage: that wait is
-    // for the MMA of an older chunk, so the MMAs never wait on the issue of the next loads.
-    bool ok = true;
-#pragma unroll 1
-    for (int q = 0; q < total; ++q) {
-      const int st = q % kStages, fill = q / kStages;
-      if (q >= kStages - 1) {
-        cp_async_wait<kStages - 2>();                          // load q - (kStages - 1) landed
-        if (gt == 0 && q >= 8 && q < 16) CSA_STAMP(10 + 3 * (q - 8));
-        complete(q - (kStages - 1));
-      }
-      if (fill > 0 && ok) ok = mbar_wait(&empty[st], (fill - 1) & 1, p.err);
-      if (gt == 0 && q >= 8 && q < 16) CSA_STAMP(11 + 3 * (q - 8));
-      if (ok) issue(q);
-      else cp_async_commit();
-      if (gt == 0 && q >= 8 && q < 16) CSA_STAMP(12 + 3 * (q - 8));
-    }
-    cp_async_wait<0>();
-#pragma unroll 1
-    for (int q = total > kStages - 1 ? total - (kStages - 1) : 0; q < total; ++q) complete(q);
+    gather(2 * n_loads);                                       // warps 6..11: phases S and O
   } else {
     // ---------------------------------------------------------------- softmax / epilogue (warps 2..5)
+    gather(n_loads);                                           // phase S, with the gather warps
     const int et = threadIdx.x - 64;                           // 0..127
     const int wq = warp & 3;
     const int r = 32 * wq + lane;                              // TMEM lane
@@ -400,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<const uint4*>(ostage + h * kTile + piece * 8);
           }
           named_barrier(1, 128);                                 // the stage is free again
+          if (et == 0) CSA_STAMP(48 + 4 * half + 2 * cc + hh);
         }
       }
     }
