@@ -192,15 +192,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   // piece u of the row range: row u / 64, 16-byte piece u % 64 (dim block (u % 64) / 8); empty rows
-  // are zero-filled (the O product reads every row up to R)
+  // are zero-filled (the O product reads every row up to R). Eight row-table reads are issued ahead
+  // of their eight copies (a copy's memory clobber would otherwise hold each read behind it).
   auto gather = [&](int r0, int r1, const __nv_bfloat16* base, int g, int ng) {
+    const int u_end = r1 * 64;
 #pragma unroll 1
-    for (int u = r0 * 64 + g; u < r1 * 64; u += ng) {
-      const int rr = u >> 6, piece = u & 63;
-      uint8_t* dst = kvs + (piece >> 3) * kBlkStride + sw128_offset(rr, piece & 7);
-      const int32_t gr = rows_s[rr];
-      if (gr >= 0) cp_async16(dst, base + (int64_t)gr * kD + piece * 8);
-      else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    for (int u0 = r0 * 64 + g; u0 < u_end; u0 += 8 * ng) {
+      int32_t gr[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int u = u0 + k * ng;
+        gr[k] = u < u_end ? rows_s[u >> 6] : -1;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int u = u0 + k * ng;
+        if (u < u_end) {
+          const int rr = u >> 6, piece = u & 63;
+          uint8_t* dst = kvs + (piece >> 3) * kBlkStride + sw128_offset(rr, piece & 7);
+          if (gr[k] >= 0) cp_async16(dst, base + (int64_t)gr[k] * kD + piece * 8);
+          else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        }
+      }
     }
     cp_async_commit();
   };

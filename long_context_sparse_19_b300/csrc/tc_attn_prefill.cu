@@ -188,15 +188,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     split_of(q, tid, nth);
     uint8_t* stage = ring + (q % kStages) * kChunkBytes;
     const __nv_bfloat16* base = j < p.win_tiles ? p.kv : p.ckv;
-    // unrolled (11 x 192 >= 2048): the row-table reads are all issued ahead of the copies
+    // 11 x 192 >= 2048 pieces: every row-table read is issued before the first copy (a copy's
+    // memory clobber would otherwise hold each read behind the previous copy)
+    int32_t g[11];
+#pragma unroll
+    for (int i = 0; i < 11; ++i) {
+      const int u = tid + i * nth;
+      g[i] = u < 2048 ? rows_s[j * kTile + (u >> 4)] : -1;
+    }
 #pragma unroll
     for (int i = 0; i < 11; ++i) {
       const int u = tid + i * nth;
       if (u < 2048) {
         const int rr = u >> 4, piece = u & 15;
         uint8_t* dst = stage + (piece >> 3) * kBlk + sw128_offset(rr, piece & 7);
-        const int32_t g = rows_s[j * kTile + rr];
-        if (g >= 0) cp_async16(dst, base + (int64_t)g * kD + c * 128 + piece * 8);
+        if (g[i] >= 0) cp_async16(dst, base + (int64_t)g[i] * kD + c * 128 + piece * 8);
         else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
       }
     }
