@@ -40,12 +40,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # profile is profiles/index_select_decode_B32_N65536.md) and scaled by 8 to B=32: every request
 # streams its own cache, so the bytes grow with B. They hold only for the kernel source they were
 # taken on: the roofline's "traffic" is null as soon as the code of any of these files differs.
-INDEX_TRAFFIC = {"bytes_per_launch": 8 * (19149568 + 0),
+INDEX_TRAFFIC = {"bytes_per_launch": 8 * (19144448 + 0),
                  "sources": ["long_context_sparse_19_b300/csrc/tc_index_select.cu",
                              "long_context_sparse_19_b300/csrc/tc_ptx.cuh",
                              "long_context_sparse_19_b300/csrc/common.cuh",
                              "long_context_sparse_19_b300/csrc/close_entry.cuh"],
-                 "sha256": "9ccbd991b8fbb972b2e104c1d2b6bf2ddb6973de38148eda0747120ad38530ff"}
+                 "sha256": "4a071f5fb49a8b2d018aa72d2c55a31696ac1504f2b3cf04b5412c70f1da1b55"}
 # GPU sleep queued ahead of each profiled step, so that the host has submitted the whole step before
 # it starts and the per-kernel events time the GPU, not the host's launch rate (~250 us at 2 GHz)
 PROFILE_SLEEP_CYCLES = 500_000
