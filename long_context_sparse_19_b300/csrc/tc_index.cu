@@ -45,6 +45,7 @@ constexpr uint32_t kBlockBytes = 16384;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kIdesc = idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdescHi = idesc_bf16(128, 64, false, false);   // the value rows only
 constexpr size_t kSmemBytes = 1024 /*align*/ + kTileBytes /*query operand*/ + kStages * kTileBytes + 512;
 
 struct IndexTcParams {
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0 && mbar_wait(qready, 0, p.err)) {
       tc_fence_after();
       const uint32_t q_addr = smem_u32(qop);
+      const bool hi_only0 = p.rope.d_rope <= kDI / 2;
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages, acc = i & 1;
         if (!mbar_wait(&full[st], (i / kStages) & 1, p.err)) break;
@@ -147,10 +149,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_after();
         const uint32_t a_addr = smem_u32(stage_base + st * kTileBytes);
         const uint32_t d = tmem + acc * 128;
+        // Dims 0..63 are not rotated when d_rope <= 64: the query there is its bf16 input, so its
+        // remainder rows are zero and those four K-slices take the value rows only (N = 64). The
+        // rotated block goes first, so that its first product initialises all 128 columns.
 #pragma unroll
-        for (int kk = 0; kk < kDI / 16; ++kk) {
+        for (int u = 0; u < kDI / 16; ++u) {
+          const int kk = (u + 4) % (kDI / 16);
           const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-          mma_bf16(d, desc_kmajor_sw128(a_addr + off), desc_kmajor_sw128(q_addr + off), kIdesc, kk > 0);
+          mma_bf16(d, desc_kmajor_sw128(a_addr + off), desc_kmajor_sw128(q_addr + off),
+                   (kk < 4 && hi_only0) ? kIdescHi : kIdesc, u > 0);
         }
         mma_commit(&empty[st]);
         mma_commit(&tfull[acc]);
