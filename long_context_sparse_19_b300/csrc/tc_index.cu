@@ -10,7 +10,8 @@
 //   * warp 1 (one lane) issues tcgen05.mma M=128 (entries) x N=128 x K=128 into a double-buffered
 //     TMEM accumulator. The N dimension holds the rotated query twice: rows 0..63 its bf16 value
 //     per head (hi) and rows 64..127 the bf16 rounding remainder (lo), so hi + lo carries the
-//     rotated fp32 query to ~16 bits and the scores keep fp32-level accuracy;
+//     rotated fp32 query to ~16 bits and the scores keep fp32-level accuracy (over the unrotated
+//     dims the remainder is zero, and those K-slices run with N=64);
 //   * warps 2..5 first build that query operand in shared memory (RoPE at t, hi/lo split,
 //     swizzled K-major layout), then run the epilogue: thread = entry, 2 x 64 TMEM columns ->
 //     sum_h w_h * relu(hi_h + lo_h) -> one coalesced fp32 score store.
